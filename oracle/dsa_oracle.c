@@ -1,0 +1,226 @@
+/*
+ * dsa_oracle.c -- plain, slow, fp64 CPU oracle of the decode-step DSA indexer.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this file's library.  The CUDA path
+ * shares no code, header, table or helper with it.
+ *
+ * What it computes (the plain definition, written out as loops):
+ *
+ *   1. live count   n_b = ceil(seq_len_b / 4)   (one C4 key per 4 tokens)
+ *   2. gather       K_b[t] = pool[page_table[b, t / E]][t % E]     t < n_b
+ *   3. score        s[b,t] = sum_h w[b,h] * max(0, sum_d q[b,h,d] * K_b[t,d])
+ *   4. mask         s[b,t] = -inf for n_b <= t < max_context / 4
+ *   5. top-k        the min(k, n_b) live positions with the largest score,
+ *                   ties to the lower position, listed in ascending position,
+ *                   padded with -1 up to k
+ *
+ * Sources.  The operator chain of the fallback indexer -- gather through the
+ * page table (copy_/index), bmm of the query against the keys, clamp_min at
+ * zero, multiply by the head weights, sum over heads, then -inf past the live
+ * length -- is given in "The Indexer O(max_context) Breakthrough" (section
+ * "The Indexer O(max_context) Breakthrough", the per-op GPU-time table and the
+ * tensor shapes that follow it) and in "The Final Piece: Documenting a ~17x
+ * Throughput Breakthrough" (section "The Context: Why This Message Was
+ * Written").  The -inf fill of a full-width row and the top-k that consumes it
+ * are described in "The O(Actual) Indexer: Validating 128K Context at 500
+ * tok/s on Blackwell" (section "The Bottleneck That Was", and "The Benchmark
+ * Results" for the top-k over the full logits).  The row width
+ * page_table.shape[1] x (page_size / 4) is from "The Moment of Breakthrough"
+ * (section "The Context: A Long Hunt for the Hidden Wall").  The pages print
+ * no formula; reading (3) puts relu on each head's dot product before the
+ * weighted head sum, the order of the quoted op chain.  The pages say nothing
+ * on ties; the lower position wins.  They give no output order for the
+ * top-k; ascending position is used.
+ *
+ * Precision.  bf16 bits widen exactly to double; w (fp32) widens exactly;
+ * every sum is accumulated in double in the order written.  The top-k
+ * compares doubles; the caller chooses whether to pass the fp64 scores or
+ * fp32 values widened to double.
+ *
+ * Layouts are C-contiguous:
+ *   q          uint16 [B, H, D]   bf16 bits
+ *   w          float  [B, H]
+ *   pool       uint16 [num_pages, E, D]  bf16 bits
+ *   page_table int32  [B, W]      W = max_context / (4 E)
+ *   seq_lens   int32  [B]         tokens
+ *   scores     double [B, M]      M = max_context / 4
+ *
+ * H, D and E are parameters (the indexer uses 32, 64, 64) so that the pins
+ * can run the definition on tiny hand-checkable shapes.
+ *
+ * Pins: every function here is checked by the non-GPU tests against closed
+ * forms, invariants, a hand-worked example and library routines.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_PAGE -1
+#define ORACLE_BAD_ARG -2
+#define ORACLE_NO_MEMORY -3
+
+/* bf16 -> double: the 16 bits are the high half of an IEEE fp32. */
+double dsa_oracle_bf16_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Step 1: C4 keys that hold data for a request of seq_len tokens. */
+int64_t dsa_oracle_live_count(int64_t seq_len)
+{
+    if (seq_len <= 0)
+        return 0;
+    return (seq_len + 3) / 4;
+}
+
+/*
+ * Step 2: contiguous keys of one request, read through its page table row.
+ * keys_out is double [n, D].  Returns ORACLE_BAD_PAGE if a live entry names
+ * a page outside the pool.
+ */
+int dsa_oracle_gather(const uint16_t *pool, int64_t num_pages, int32_t E, int32_t D,
+                      const int32_t *table_row, int64_t W, int64_t n, double *keys_out)
+{
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t j = t / E;  /* page slot in the table row */
+        int64_t e = t % E;  /* entry inside the page */
+        if (j >= W)
+            return ORACLE_BAD_ARG;
+        int64_t page = table_row[j];
+        if (page < 0 || page >= num_pages)
+            return ORACLE_BAD_PAGE;
+        const uint16_t *src = pool + (page * E + e) * D;
+        for (int32_t d = 0; d < D; ++d)
+            keys_out[t * D + d] = dsa_oracle_bf16_to_double(src[d]);
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Steps 3 and 4 on contiguous keys: one request, row of M positions.
+ * q_row uint16 [H, D], w_row float [H], keys double [n, D], out double [M].
+ */
+void dsa_oracle_scores_dense(const uint16_t *q_row, const float *w_row, int32_t H, int32_t D,
+                             const double *keys, int64_t n, int64_t M, double *out)
+{
+    for (int64_t t = 0; t < M; ++t) {
+        if (t >= n) {
+            out[t] = -INFINITY;
+            continue;
+        }
+        double s = 0.0;
+        for (int32_t h = 0; h < H; ++h) {
+            double dot = 0.0;
+            for (int32_t d = 0; d < D; ++d)
+                dot += dsa_oracle_bf16_to_double(q_row[h * D + d]) * keys[t * D + d];
+            double r = dot > 0.0 ? dot : 0.0;
+            s += (double)w_row[h] * r;
+        }
+        out[t] = s;
+    }
+}
+
+/*
+ * Steps 1-4 for a batch: scores double [B, M], M = max_context / 4.
+ * A sequence length above max_context is an argument error here (the oracle
+ * is only run on in-contract inputs).
+ */
+int dsa_oracle_scores(const uint16_t *q, const float *w, int32_t H, int32_t D,
+                      const uint16_t *pool, int64_t num_pages, int32_t E,
+                      const int32_t *page_table, const int32_t *seq_lens, int32_t B,
+                      int64_t max_context, double *scores)
+{
+    if (B < 0 || H <= 0 || D <= 0 || E <= 0 || max_context <= 0 || max_context % (4 * E) != 0)
+        return ORACLE_BAD_ARG;
+    int64_t M = max_context / 4;
+    int64_t W = max_context / (4 * E);
+    double *keys = (double *)malloc((size_t)(M > 0 ? M : 1) * (size_t)D * sizeof(double));
+    if (!keys)
+        return ORACLE_NO_MEMORY;
+    int rc = ORACLE_OK;
+    for (int32_t b = 0; b < B; ++b) {
+        if (seq_lens[b] > max_context) {
+            rc = ORACLE_BAD_ARG;
+            break;
+        }
+        int64_t n = dsa_oracle_live_count(seq_lens[b]);
+        rc = dsa_oracle_gather(pool, num_pages, E, D, page_table + (int64_t)b * W, W, n, keys);
+        if (rc != ORACLE_OK)
+            break;
+        dsa_oracle_scores_dense(q + (int64_t)b * H * D, w + (int64_t)b * H, H, D, keys, n, M,
+                                scores + (int64_t)b * M);
+    }
+    free(keys);
+    return rc;
+}
+
+typedef struct {
+    double s;
+    int64_t t;
+} scored_pos;
+
+/* Larger score first; equal scores: lower position first. */
+static int by_score_then_position(const void *a, const void *b)
+{
+    const scored_pos *x = (const scored_pos *)a, *y = (const scored_pos *)b;
+    if (x->s > y->s)
+        return -1;
+    if (x->s < y->s)
+        return 1;
+    return (x->t > y->t) - (x->t < y->t);
+}
+
+static int ascending_i32(const void *a, const void *b)
+{
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+/*
+ * Step 5 for one row: full sort of the n live positions by (score desc,
+ * position asc), keep the first min(k, n), list them in ascending position,
+ * pad with -1.  out int32 [k].
+ */
+int dsa_oracle_topk_row(const double *row, int64_t n, int32_t k, int32_t *out)
+{
+    if (k <= 0 || n < 0)
+        return ORACLE_BAD_ARG;
+    int64_t keep = n < (int64_t)k ? n : (int64_t)k;
+    scored_pos *all = (scored_pos *)malloc((size_t)(n > 0 ? n : 1) * sizeof(scored_pos));
+    if (!all)
+        return ORACLE_NO_MEMORY;
+    for (int64_t t = 0; t < n; ++t) {
+        all[t].s = row[t];
+        all[t].t = t;
+    }
+    qsort(all, (size_t)n, sizeof(scored_pos), by_score_then_position);
+    for (int64_t i = 0; i < keep; ++i)
+        out[i] = (int32_t)all[i].t;
+    qsort(out, (size_t)keep, sizeof(int32_t), ascending_i32);
+    for (int64_t i = keep; i < k; ++i)
+        out[i] = -1;
+    free(all);
+    return ORACLE_OK;
+}
+
+/* Step 5 for a batch: rows double [B, M], topk int32 [B, k]. */
+int dsa_oracle_topk(const double *rows, const int32_t *seq_lens, int32_t B, int64_t max_context,
+                    int32_t k, int32_t *topk)
+{
+    int64_t M = max_context / 4;
+    for (int32_t b = 0; b < B; ++b) {
+        int64_t n = dsa_oracle_live_count(seq_lens[b]);
+        if (n > M)
+            return ORACLE_BAD_ARG;
+        int rc = dsa_oracle_topk_row(rows + (int64_t)b * M, n, k, topk + (int64_t)b * k);
+        if (rc != ORACLE_OK)
+            return rc;
+    }
+    return ORACLE_OK;
+}

@@ -1,0 +1,141 @@
+"""ctypes front-end of the fp64 CPU oracle (``dsa_oracle.c``).
+
+TEST INFRASTRUCTURE.  Only the test suite, the package smoke check and the
+benchmark's CPU-baseline leg may import this module.  It never touches the
+CUDA library and the CUDA library never touches it.
+
+``build()`` compiles ``dsa_oracle.c`` with gcc (strict IEEE: no fast-math, no
+contraction of multiply-add) into ``liboracle_dsa.so`` beside it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "dsa_oracle.c")
+LIB = os.path.join(HERE, "liboracle_dsa.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+        tmp = LIB + f".{os.getpid()}.tmp"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+               "-fno-fast-math", SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, LIB)
+    return LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(LIB)
+        i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+        lib.dsa_oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.dsa_oracle_bf16_to_double.restype = ctypes.c_double
+        lib.dsa_oracle_live_count.argtypes = [i64]
+        lib.dsa_oracle_live_count.restype = i64
+        lib.dsa_oracle_gather.argtypes = [p, i64, i32, i32, p, i64, i64, p]
+        lib.dsa_oracle_gather.restype = ctypes.c_int
+        lib.dsa_oracle_scores_dense.argtypes = [p, p, i32, i32, p, i64, i64, p]
+        lib.dsa_oracle_scores_dense.restype = None
+        lib.dsa_oracle_scores.argtypes = [p, p, i32, i32, p, i64, i32, p, p, i32, i64, p]
+        lib.dsa_oracle_scores.restype = ctypes.c_int
+        lib.dsa_oracle_topk_row.argtypes = [p, i64, i32, p]
+        lib.dsa_oracle_topk_row.restype = ctypes.c_int
+        lib.dsa_oracle_topk.argtypes = [p, p, i32, i64, i32, p]
+        lib.dsa_oracle_topk.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags.c_contiguous
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with code {rc}")
+
+
+def bf16_to_double(bits: int) -> float:
+    return float(_load().dsa_oracle_bf16_to_double(int(bits)))
+
+
+def live_count(seq_len: int) -> int:
+    return int(_load().dsa_oracle_live_count(int(seq_len)))
+
+
+def gather(pool, table_row, n: int, entries: int = 64) -> np.ndarray:
+    """Contiguous fp64 keys [n, D] of one request read through its table row."""
+    pool = np.ascontiguousarray(pool, dtype=np.uint16)
+    table_row = np.ascontiguousarray(table_row, dtype=np.int32)
+    D = pool.shape[-1]
+    out = np.empty((max(n, 0), D), dtype=np.float64)
+    rc = _load().dsa_oracle_gather(_ptr(pool), pool.shape[0], entries, D, _ptr(table_row),
+                                   table_row.shape[0], n, _ptr(out))
+    _check(rc, "gather")
+    return out
+
+
+def scores_dense(q_row, w_row, keys, row_width: int) -> np.ndarray:
+    """fp64 scores of one request over contiguous keys; -inf from len(keys) on."""
+    q_row = np.ascontiguousarray(q_row, dtype=np.uint16)
+    w_row = np.ascontiguousarray(w_row, dtype=np.float32)
+    keys = np.ascontiguousarray(keys, dtype=np.float64)
+    H, D = q_row.shape
+    out = np.empty(row_width, dtype=np.float64)
+    _load().dsa_oracle_scores_dense(_ptr(q_row), _ptr(w_row), H, D, _ptr(keys), keys.shape[0],
+                                    row_width, _ptr(out))
+    return out
+
+
+def scores(q, w, key_pool, page_table, seq_lens, max_context: int) -> np.ndarray:
+    """fp64 scores [B, max_context/4] through the page table."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    pool = np.ascontiguousarray(key_pool, dtype=np.uint16)
+    table = np.ascontiguousarray(page_table, dtype=np.int32)
+    seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, H, D = q.shape
+    E = pool.shape[1]
+    out = np.empty((B, max_context // 4), dtype=np.float64)
+    rc = _load().dsa_oracle_scores(_ptr(q), _ptr(w), H, D, _ptr(pool), pool.shape[0], E,
+                                   _ptr(table), _ptr(seq), B, max_context, _ptr(out))
+    _check(rc, "scores")
+    return out
+
+
+def topk_row(row, n: int, k: int) -> np.ndarray:
+    row = np.ascontiguousarray(row, dtype=np.float64)
+    out = np.empty(k, dtype=np.int32)
+    _check(_load().dsa_oracle_topk_row(_ptr(row), n, k, _ptr(out)), "topk_row")
+    return out
+
+
+def topk(rows, seq_lens, max_context: int, k: int) -> np.ndarray:
+    """Top-k [B, k] of score rows [B, max_context/4] (any float dtype, widened)."""
+    rows = np.ascontiguousarray(rows, dtype=np.float64)
+    seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B = rows.shape[0]
+    out = np.empty((B, k), dtype=np.int32)
+    _check(_load().dsa_oracle_topk(_ptr(rows), _ptr(seq), B, max_context, k, _ptr(out)), "topk")
+    return out
+
+
+def case_scores(case) -> np.ndarray:
+    return scores(case.q, case.w, case.key_pool, case.page_table, case.seq_lens, case.max_context)
+
+
+def case_topk(case, rows=None) -> np.ndarray:
+    if rows is None:
+        rows = case_scores(case)
+    return topk(rows, case.seq_lens, case.max_context, case.k)
