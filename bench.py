@@ -1,0 +1,382 @@
+"""Throughput of the decode-step DSA indexer on one GB300 (or N replicas).
+
+One step = one pass of the whole indexer over one decode batch: the scores
+kernel (page-table lookup, page gather, QK on the tensor cores, relu-weighted
+head sum, -inf fill of the full-width row) followed by the top-k kernel, both
+through the C ABI.  Default workload: B=64 requests, 128K max context, every
+request 131072 tokens long (32768 live C4 positions per row), keys with 1%
+x8 outliers, k=2048, 32768 distinct pages in a shuffled pool (268 MB of live
+keys, twice the L2).  The metric is live C4 positions scored and selected per
+second; the roofline is live key bytes / scores-kernel time against the
+measured HBM copy bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica of the workload on its own GPU
+(weak scaling, no data-path collective); rank 0 prints one JSON line.
+``--impl reference`` times the fp64 CPU oracle on the host cores on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "C4 positions scored+top-k per sec and HBM GB/s (% of roofline), B=64 @128K"
+UNIT = "positions/s"
+KEY_BYTES_PER_POSITION = 128          # 64 bf16 dims of one C4 index key
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20               # > 2x the 129 MB L2
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "scores_kernel_b64_ctx128k_dense.md")
+SCORES_SRC = os.path.join(ROOT, "sparse_attention_paged_dsa_gb300", "csrc", "scores_kernel.cu")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="b64_ctx128k_dense")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-sample-rows", type=int, default=32,
+                    help="rows of the workload the CPU baseline times (about 10-30 s on one core)")
+    ap.add_argument("--reference-rows-per-step", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ ranks
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_units: float, local_seconds: float, group=None):
+    """Whole-job units and the slowest rank's time (max over ranks)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return local_units, local_seconds
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    s = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX, group=group)
+    return float(u.item()), float(s.item())
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        else:
+            self.lines = []
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- helpers
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per scores launch from the committed ncu summary, if the kernel is unchanged."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    sha = hashlib.sha256(open(SCORES_SRC, "rb").read()).hexdigest()
+    fields = dict(l.split(":", 1) for l in text.splitlines() if l.startswith(("source_sha256:", "dram_bytes_per_launch:")))
+    if fields.get("source_sha256", "").strip() != sha:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
+def cpu_baseline(case, rows: int):
+    """The fp64 oracle as it stands, single-threaded, on `rows` rows of the workload."""
+    from oracle import oracle
+    oracle.build()
+    rows = max(1, min(rows, case.batch))
+    from sparse_attention_paged_dsa_gb300.inputs import IndexerCase
+    sub = IndexerCase("sample", case.q[:rows], case.w[:rows], case.key_pool, case.page_table[:rows],
+                      case.seq_lens[:rows], case.max_context, case.k)
+    t0 = time.perf_counter()
+    s = oracle.case_scores(sub)
+    oracle.case_topk(sub, s)
+    dt = time.perf_counter() - t0
+    pos = int(sub.live_positions().sum())
+    return {"value": pos / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} of {case.batch} rows ({pos} live positions), fp64 scores + full-sort top-k, "
+                      f"{dt:.2f} s"}
+
+
+def workload_config(case, world):
+    live = int(case.live_positions().sum())
+    return {"workload": case.name, "batch": case.batch, "max_context": case.max_context,
+            "seq_len": int(case.seq_lens.max()), "k": case.k, "pool_pages": case.num_pages,
+            "live_positions": live, "live_key_bytes": live * KEY_BYTES_PER_POSITION,
+            "l2": "flushed between steps (512 MiB memset, outside the events); inputs 2x L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+# ----------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from sparse_attention_paged_dsa_gb300 import inputs
+    case = inputs.workload(args.workload)
+    from oracle import oracle
+    oracle.build()
+    from sparse_attention_paged_dsa_gb300.inputs import IndexerCase
+    r = max(1, min(args.reference_rows_per_step, case.batch))
+
+    def step(i):
+        b0 = (i * r) % case.batch
+        idx = [(b0 + j) % case.batch for j in range(r)]
+        sub = IndexerCase("sample", case.q[idx], case.w[idx], case.key_pool, case.page_table[idx],
+                          case.seq_lens[idx], case.max_context, case.k)
+        s = oracle.case_scores(sub)
+        oracle.case_topk(sub, s)
+        return int(sub.live_positions().sum())
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    pos = sum(step(args.warmup + i) for i in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = pos / dt
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(case, 1), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{r} rows of {case.batch} per step (fp64 oracle, one host core)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+
+    from sparse_attention_paged_dsa_gb300 import binding, inputs
+    binding.load()
+    case = inputs.workload(args.workload)
+    B, M, K = case.batch, case.max_context // 4, case.k
+    live = int(case.live_positions().sum())
+
+    q, w, pool, table, seq = binding.to_device(case, device)
+    scores = torch.empty((B, M), dtype=torch.float32, device=device)
+    topk = torch.empty((B, K), dtype=torch.int32, device=device)
+    ws = binding.new_workspace(B, case.max_context, K, device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        binding.dsa_indexer_scores(q, w, pool, table, seq, case.max_context, scores=scores, workspace=ws)
+        binding.dsa_indexer_topk(scores, seq, case.max_context, K, topk_idx=topk, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    if binding.get_error(ws) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    with ClockSampler(device.index) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+        clocks.mark_start()
+        wall0 = time.perf_counter()
+        for i in range(n):
+            flush.zero_()
+            ev[i][0].record(stream)
+            binding.dsa_indexer_scores(q, w, pool, table, seq, case.max_context, scores=scores, workspace=ws)
+            ev[i][1].record(stream)
+            binding.dsa_indexer_topk(scores, seq, case.max_context, K, topk_idx=topk, workspace=ws)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(device)
+        if world > 1:
+            dist.barrier()
+        wall1 = time.perf_counter()
+        clocks.mark_end()
+    t_scores = [e[0].elapsed_time(e[1]) * 1e-3 for e in ev]
+    t_topk = [e[1].elapsed_time(e[2]) * 1e-3 for e in ev]
+    t_step = [e[0].elapsed_time(e[2]) * 1e-3 for e in ev]
+    local_seconds = sum(t_step)
+    total_units, max_seconds = aggregate(live * n, local_seconds)
+    value = total_units / max_seconds
+    if binding.get_error(ws) != 0:
+        raise RuntimeError("device error word set during the timed steps")
+
+    # e2e: host (pinned) inputs -> device, both calls, top-k back to the host, every step.
+    host = [torch.from_numpy(a).pin_memory() for a in
+            (case.q.view("int16"), case.w, case.key_pool.view("int16"), case.page_table, case.seq_lens)]
+    dev_in = [torch.empty(h.shape, dtype=h.dtype, device=device) for h in host]
+    out_host = torch.empty((B, K), dtype=torch.int32).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for d, h in zip(dev_in, host):
+            d.copy_(h, non_blocking=True)
+        qd, wd, pd, td, sd = dev_in
+        binding.dsa_indexer_scores(qd.view(torch.bfloat16), wd, pd.view(torch.bfloat16), td, sd,
+                                   case.max_context, scores=scores, workspace=ws)
+        binding.dsa_indexer_topk(scores, sd, case.max_context, K, topk_idx=topk, workspace=ws)
+        out_host.copy_(topk, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_units, e2e_seconds = aggregate(live * args.e2e_steps, e0.elapsed_time(e1) * 1e-3)
+    if not np.array_equal(out_host.numpy(), topk.cpu().numpy()):
+        raise RuntimeError("e2e top-k read-back mismatch")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, args.cpu_sample_rows)
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    peak, peak_kind = measured_hbm_peak()
+    mean_scores = statistics.fmean(t_scores)
+    achieved = live * KEY_BYTES_PER_POSITION / mean_scores / 1e9
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.fmean(t_step), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(case, world),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": "scores_kernel",
+                     "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
+                     "algorithmic_bytes_per_launch": live * KEY_BYTES_PER_POSITION},
+        "kernels_us": {"scores_mean": 1e6 * mean_scores, "scores_median": 1e6 * statistics.median(t_scores),
+                       "topk_mean": 1e6 * statistics.fmean(t_topk),
+                       "step_p10": 1e6 * float(np.percentile(t_step, 10)),
+                       "step_p50": 1e6 * float(np.percentile(t_step, 50)),
+                       "step_p90": 1e6 * float(np.percentile(t_step, 90))},
+        "step_gbs_live_keys": live * KEY_BYTES_PER_POSITION / statistics.fmean(t_step) / 1e9,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_units / e2e_seconds, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * n * world,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": wall1 - wall0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

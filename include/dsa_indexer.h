@@ -1,0 +1,162 @@
+/*
+ * dsa_indexer.h -- C ABI of the GB300 (sm_103a) decode-step DSA indexer.
+ *
+ * For each request b of a decode batch the indexer
+ *   1. reads the request's C4-compressed 64-dim index keys (one key per 4
+ *      tokens, 64 keys per 256-token page) through its row of the page table;
+ *   2. scores every live position t < n_b = ceil(seq_len_b / 4):
+ *          score[b, t] = sum_{h < 32} w[b, h] * max(0, q[b, h, :] . k[t, :]);
+ *   3. writes -inf into the rest of a full-width row of max_context / 4
+ *      positions;
+ *   4. selects the min(k, n_b) live positions with the largest scores.
+ *
+ * Where each step is defined:
+ *   - the operator chain (gather through the page table, bmm of q against
+ *     the keys, clamp_min at 0, multiply by the head weights, sum over heads,
+ *     -inf past the live length) and the 32-head, 64-dim shapes:
+ *     "The Indexer O(max_context) Breakthrough", section "The Indexer
+ *     O(max_context) Breakthrough" (per-op table and tensor shapes), and
+ *     "The Final Piece: Documenting a ~17x Throughput Breakthrough", section
+ *     "The Context: Why This Message Was Written";
+ *   - row width = page_table width x (page_size / 4):
+ *     "The Moment of Breakthrough: Validating the Indexer Fix That Unlocked
+ *     17x Throughput on Blackwell", section "The Context: A Long Hunt for the
+ *     Hidden Wall";
+ *   - a fixed grid whose pages past the live length take a cheap -inf path,
+ *     with a full-size output row for the downstream top-k and for CUDA-graph
+ *     capture: "The O(Actual) Indexer: Validating 128K Context at 500 tok/s on
+ *     Blackwell", section "The Bottleneck That Was";
+ *   - the top-k over the logits row that feeds sparse attention: same page,
+ *     sections "The Benchmark Results" and "The Reasoning Process".
+ * The pages print no formula, no tie rule and no output order.  Readings used
+ * here: relu acts on each head's dot product before the weighted head sum;
+ * equal scores are ranked by lower position; top-k indices are listed in
+ * ascending position, then padded with -1.
+ *
+ * Conventions shared by every entry point:
+ *   - Device pointers unless stated otherwise; all buffers are owned by the
+ *     caller.  The library allocates, frees and synchronises nothing inside a
+ *     compute call, so every compute call may be captured in a CUDA graph.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls are asynchronous on it.
+ *   - The launch configuration depends only on (batch, max_context, k) and the
+ *     device, never on the contents of seq_lens or page_table, so a captured
+ *     graph stays valid when those contents change between replays.
+ *   - Arguments are checked on the host before any launch; a failed check
+ *     returns a status and launches nothing.  No C++ exception crosses the ABI.
+ *   - Fixed shape: 32 heads, head dim 64, 64 C4 entries (256 tokens) per page.
+ *   - Layouts (C-contiguous):
+ *       q          bf16  [batch, 32, 64]                 16-byte aligned
+ *       w          fp32  [batch, 32]                     16-byte aligned
+ *       key_pool   bf16  [num_pages, 64, 64]  (page, entry, dim), 16-byte aligned
+ *       page_table int32 [batch, max_context / 256]       physical page ids
+ *       seq_lens   int32 [batch]                          tokens per request
+ *       scores     fp32  [batch, max_context / 4]         16-byte aligned
+ *       topk_idx   int32 [batch, k]
+ *   - Page-table entries at or past slot ceil(n_b / 64) are never read.
+ *   - Device data out of contract is never dereferenced: a seq_len above
+ *     max_context is treated as max_context and a negative one as 0; a live
+ *     page id outside [0, num_pages) is not read and its positions score -inf.
+ *     Each case sets a bit in the workspace error word (DSA_DEVERR_*).
+ *   - Workspace: a caller-owned device buffer of at least
+ *     dsa_indexer_workspace_size() bytes, zeroed once before first use
+ *     (dsa_indexer_workspace_init or any memset to 0).  Its first 256 bytes
+ *     hold the sticky device error word.  Calls that share a workspace must
+ *     be ordered on one stream.
+ */
+#ifndef DSA_INDEXER_H
+#define DSA_INDEXER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or shape */
+    DSA_ERR_UNSUPPORTED = 2, /* shape outside what the kernels handle (e.g. batch too large) */
+    DSA_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
+    DSA_ERR_CUDA = 4         /* a CUDA runtime/driver call failed; see dsa_indexer_last_cuda_error */
+} dsa_status_t;
+
+/* Bits of the device error word (sticky until read with clear = 1). */
+#define DSA_DEVERR_SEQ_LEN_CLAMPED 0x1u /* a seq_len was < 0 or > max_context */
+#define DSA_DEVERR_BAD_PAGE        0x2u /* a live page id was outside [0, num_pages) */
+#define DSA_DEVERR_WAIT_TIMEOUT    0x4u /* an in-kernel pipeline wait gave up (about 1 s) */
+
+#define DSA_HEADS 32
+#define DSA_HEAD_DIM 64
+#define DSA_PAGE_TOKENS 256
+#define DSA_PAGE_ENTRIES 64
+#define DSA_MAX_BATCH 1024
+
+/*
+ * Bytes of workspace any entry point needs for this shape: 256 bytes of
+ * header plus, for dsa_indexer_fused without a scores row, batch x
+ * max_context / 4 fp32 live-score slots (only live positions are touched).
+ * Returns 0 for an invalid shape.
+ */
+DSA_API size_t dsa_indexer_workspace_size(int32_t batch, int64_t max_context, int32_t k);
+
+/* Zero the workspace header (error word) on `stream`.  Capture-safe. */
+DSA_API dsa_status_t dsa_indexer_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Steps 1-3: scores [batch, max_context / 4], every position written (live
+ * scores, -inf elsewhere).  Cost: live key bytes, plus one streaming -inf store
+ * per dead position (the full-width row).
+ */
+DSA_API dsa_status_t dsa_indexer_scores(const void *q, const float *w, const void *key_pool,
+                                int64_t num_pages, const int32_t *page_table,
+                                const int32_t *seq_lens, int32_t batch, int64_t max_context,
+                                float *scores, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/*
+ * Step 4 on a scores row: topk_idx [batch, k] = the min(k, n_b) positions
+ * t < n_b with the largest scores[b, t] (fp32 order; equal scores: lower t
+ * first), in ascending t, then -1.  Reads only scores[b, t] for t < n_b, and
+ * none when n_b <= k.  1 <= k <= max_context / 4.
+ */
+DSA_API dsa_status_t dsa_indexer_topk(const float *scores, const int32_t *seq_lens, int32_t batch,
+                              int64_t max_context, int32_t k, int32_t *topk_idx,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Steps 1-4.  With scores_opt != NULL the full-width row is written exactly as
+ * by dsa_indexer_scores and topk_idx equals dsa_indexer_topk on it.  With
+ * scores_opt == NULL nothing of size max_context is written: live scores go to
+ * the workspace and the cost is O(live positions) plus O(batch x k).
+ */
+DSA_API dsa_status_t dsa_indexer_fused(const void *q, const float *w, const void *key_pool,
+                               int64_t num_pages, const int32_t *page_table,
+                               const int32_t *seq_lens, int32_t batch, int64_t max_context,
+                               int32_t k, int32_t *topk_idx, float *scores_opt,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Read the sticky device error word into *code (host pointer).  Synchronises
+ * `stream` (not capture-safe).  clear != 0 zeroes the word afterwards.
+ */
+DSA_API dsa_status_t dsa_indexer_get_error(void *workspace, uint32_t *code, int clear, void *stream);
+
+/* Static string for a status code. */
+DSA_API const char *dsa_status_string(dsa_status_t status);
+
+/* Text of the last CUDA error this thread saw inside the library ("" if none). */
+DSA_API const char *dsa_indexer_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_INDEXER_H */

@@ -1,0 +1,189 @@
+"""Thin Python front-end of ``libdsa_indexer.so`` (argument marshalling only).
+
+Every function here checks tensor dtypes, shapes and devices, then calls the
+C entry point of the same name with raw device pointers and the current
+torch CUDA stream.  All indexer arithmetic runs in the library's CUDA
+kernels; if the library has not been built, ``load()`` raises instead of
+falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdsa_indexer.so")
+
+HEADS, HEAD_DIM, PAGE_ENTRIES, PAGE_TOKENS = 32, 64, 64, 256
+WORKSPACE_HEADER_BYTES = 256
+
+DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE, DSA_ERR_CUDA = range(5)
+DEVERR_SEQ_LEN_CLAMPED, DEVERR_BAD_PAGE, DEVERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4
+
+_lib = None
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = load()
+        msg = lib.dsa_status_string(status).decode()
+        if status == DSA_ERR_CUDA:
+            msg += ": " + lib.dsa_indexer_last_cuda_error().decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+def load():
+    """Load the CUDA library (built by ``build.build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    st = ctypes.c_int
+    lib.dsa_indexer_workspace_size.argtypes = [i32, i64, i32]
+    lib.dsa_indexer_workspace_size.restype = sz
+    lib.dsa_indexer_workspace_init.argtypes = [p, sz, p]
+    lib.dsa_indexer_workspace_init.restype = st
+    lib.dsa_indexer_scores.argtypes = [p, p, p, i64, p, p, i32, i64, p, p, sz, p]
+    lib.dsa_indexer_scores.restype = st
+    lib.dsa_indexer_topk.argtypes = [p, p, i32, i64, i32, p, p, sz, p]
+    lib.dsa_indexer_topk.restype = st
+    lib.dsa_indexer_fused.argtypes = [p, p, p, i64, p, p, i32, i64, i32, p, p, p, sz, p]
+    lib.dsa_indexer_fused.restype = st
+    lib.dsa_indexer_get_error.argtypes = [p, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, p]
+    lib.dsa_indexer_get_error.restype = st
+    lib.dsa_status_string.argtypes = [st]
+    lib.dsa_status_string.restype = ctypes.c_char_p
+    lib.dsa_indexer_last_cuda_error.argtypes = []
+    lib.dsa_indexer_last_cuda_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtypes, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
+
+
+def workspace_size(batch: int, max_context: int, k: int = 1) -> int:
+    return int(load().dsa_indexer_workspace_size(batch, max_context, k))
+
+
+def new_workspace(batch: int, max_context: int, k: int = 1, device="cuda") -> torch.Tensor:
+    """A zeroed workspace of the size every entry point accepts for this shape."""
+    n = workspace_size(batch, max_context, k)
+    if n == 0:
+        raise ValueError("invalid shape for a workspace")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def _check(status: int, where: str):
+    if status != DSA_OK:
+        raise DsaError(status, where)
+
+
+def _score_args(q, w, key_pool, page_table, seq_lens, max_context):
+    B = q.shape[0]
+    _need(q, "q", _BF16, (B, HEADS, HEAD_DIM))
+    _need(w, "w", (torch.float32,), (B, HEADS))
+    _need(key_pool, "key_pool", _BF16)
+    if key_pool.dim() != 3 or tuple(key_pool.shape[1:]) != (PAGE_ENTRIES, HEAD_DIM):
+        raise ValueError(f"key_pool must be [num_pages, 64, 64], got {tuple(key_pool.shape)}")
+    _need(page_table, "page_table", (torch.int32,), (B, max_context // PAGE_TOKENS))
+    _need(seq_lens, "seq_lens", (torch.int32,), (B,))
+    return B
+
+
+def dsa_indexer_scores(q, w, key_pool, page_table, seq_lens, max_context: int, scores=None, workspace=None):
+    """Scores [B, max_context/4] fp32: live scores, -inf elsewhere."""
+    B = _score_args(q, w, key_pool, page_table, seq_lens, max_context)
+    M = max_context // 4
+    if scores is None:
+        scores = torch.empty((B, M), dtype=torch.float32, device=q.device)
+    _need(scores, "scores", (torch.float32,), (B, M))
+    if workspace is None:
+        workspace = torch.zeros(WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=q.device)
+    st = load().dsa_indexer_scores(_ptr(q), _ptr(w), _ptr(key_pool), key_pool.shape[0], _ptr(page_table),
+                                   _ptr(seq_lens), B, max_context, _ptr(scores), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(q.device))
+    _check(st, "dsa_indexer_scores")
+    return scores
+
+
+def dsa_indexer_topk(scores, seq_lens, max_context: int, k: int, topk_idx=None, workspace=None):
+    """Top-k positions [B, k] int32 of each row's live scores (ascending, -1 padded)."""
+    B = scores.shape[0]
+    _need(scores, "scores", (torch.float32,), (B, max_context // 4))
+    _need(seq_lens, "seq_lens", (torch.int32,), (B,))
+    if topk_idx is None:
+        topk_idx = torch.empty((B, k), dtype=torch.int32, device=scores.device)
+    _need(topk_idx, "topk_idx", (torch.int32,), (B, k))
+    if workspace is None:
+        workspace = torch.zeros(WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=scores.device)
+    st = load().dsa_indexer_topk(_ptr(scores), _ptr(seq_lens), B, max_context, k, _ptr(topk_idx), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(scores.device))
+    _check(st, "dsa_indexer_topk")
+    return topk_idx
+
+
+def dsa_indexer_fused(q, w, key_pool, page_table, seq_lens, max_context: int, k: int, topk_idx=None,
+                      scores=None, workspace=None):
+    """Scores + top-k in one call; ``scores`` None keeps the full-width row unwritten."""
+    B = _score_args(q, w, key_pool, page_table, seq_lens, max_context)
+    if topk_idx is None:
+        topk_idx = torch.empty((B, k), dtype=torch.int32, device=q.device)
+    _need(topk_idx, "topk_idx", (torch.int32,), (B, k))
+    if scores is not None:
+        _need(scores, "scores", (torch.float32,), (B, max_context // 4))
+    if workspace is None:
+        workspace = new_workspace(B, max_context, k, q.device)
+    st = load().dsa_indexer_fused(_ptr(q), _ptr(w), _ptr(key_pool), key_pool.shape[0], _ptr(page_table),
+                                  _ptr(seq_lens), B, max_context, k, _ptr(topk_idx), _ptr(scores),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(q.device))
+    _check(st, "dsa_indexer_fused")
+    return topk_idx
+
+
+def get_error(workspace, clear: bool = True) -> int:
+    """Read (and by default clear) the sticky device error word; synchronises the stream."""
+    code = ctypes.c_uint32(0)
+    st = load().dsa_indexer_get_error(_ptr(workspace), ctypes.byref(code), int(bool(clear)),
+                                      _stream(workspace.device))
+    _check(st, "dsa_indexer_get_error")
+    return int(code.value)
+
+
+def to_device(case, device="cuda"):
+    """Copy an ``inputs.IndexerCase`` to device tensors (q, w, key_pool, page_table, seq_lens)."""
+    q = torch.from_numpy(case.q.view("int16")).to(device).view(torch.bfloat16)
+    w = torch.from_numpy(case.w).to(device)
+    pool = torch.from_numpy(case.key_pool.view("int16")).to(device).view(torch.bfloat16)
+    table = torch.from_numpy(case.page_table).to(device)
+    seq = torch.from_numpy(case.seq_lens).to(device)
+    return q, w, pool, table, seq

@@ -1,0 +1,239 @@
+// dsa_indexer_api.cu -- the C ABI (include/dsa_indexer.h): argument checks,
+// TMA descriptor set-up, and kernel launches on the caller's stream.
+// Nothing here allocates, frees or synchronises during a compute call.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/dsa_indexer.h"
+#include "indexer_kernels.h"
+
+namespace {
+
+using dsa::kHeadDim;
+using dsa::kHeads;
+using dsa::kPageEntries;
+
+constexpr int64_t kMaxContext = int64_t(1) << 24;  // 16M tokens per request row
+constexpr int64_t kMaxPages = (int64_t(1) << 31) - 1;
+
+thread_local char g_last_cuda_error[256] = "";
+
+dsa_status_t cuda_fail(cudaError_t e, const char* where) {
+    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s (%d)", where, cudaGetErrorString(e),
+                  int(e));
+    return DSA_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// Key pool [num_pages, 64, 64] bf16 as a 3-D tensor (dim, entry, page); one
+// box = one whole page, stored with the 128-byte swizzle the MMA reads.
+dsa_status_t make_keys_map(CUtensorMap* map, const void* key_pool, int64_t num_pages) {
+    auto enc = encode_tiled();
+    if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled lookup");
+    const cuuint64_t dims[3] = {cuuint64_t(kHeadDim), cuuint64_t(kPageEntries), cuuint64_t(num_pages)};
+    const cuuint64_t strides[2] = {cuuint64_t(kHeadDim * 2), cuuint64_t(kPageEntries * kHeadDim * 2)};
+    const cuuint32_t box[3] = {cuuint32_t(kHeadDim), cuuint32_t(kPageEntries), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(key_pool), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled(keys): CUresult %d",
+                      int(r));
+        return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+}
+
+// Query [batch * 32, 64] bf16; one box = the 32 heads of one request.
+dsa_status_t make_q_map(CUtensorMap* map, const void* q, int32_t batch) {
+    auto enc = encode_tiled();
+    if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled lookup");
+    const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), cuuint64_t(batch) * kHeads};
+    const cuuint64_t strides[1] = {cuuint64_t(kHeadDim * 2)};
+    const cuuint32_t box[2] = {cuuint32_t(kHeadDim), cuuint32_t(kHeads)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled(q): CUresult %d",
+                      int(r));
+        return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+}
+
+dsa_status_t check_shape(int32_t batch, int64_t max_context) {
+    if (batch < 1 || max_context < 1 || max_context % DSA_PAGE_TOKENS != 0) return DSA_ERR_INVALID_ARG;
+    if (batch > DSA_MAX_BATCH || max_context > kMaxContext) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+dsa_status_t check_workspace(const void* ws, size_t bytes, size_t need) {
+    if (ws == nullptr || !aligned(ws, 256) || bytes < need) return DSA_ERR_WORKSPACE;
+    return DSA_OK;
+}
+
+dsa_status_t check_score_inputs(const void* q, const float* w, const void* key_pool, int64_t num_pages,
+                                const int32_t* page_table, const int32_t* seq_lens) {
+    if (!q || !w || !key_pool || !page_table || !seq_lens) return DSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(w, 16) || !aligned(key_pool, 16) || !aligned(page_table, 4) ||
+        !aligned(seq_lens, 4))
+        return DSA_ERR_INVALID_ARG;
+    if (num_pages < 1 || num_pages > kMaxPages) return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+}
+
+dsa_status_t run_scores(const void* q, const float* w, const void* key_pool, int64_t num_pages,
+                        const int32_t* page_table, const int32_t* seq_lens, int32_t batch, int64_t max_context,
+                        float* out, int fill_dead, void* workspace, cudaStream_t stream) {
+    CUtensorMap keys_map, q_map;
+    dsa_status_t st = make_keys_map(&keys_map, key_pool, num_pages);
+    if (st != DSA_OK) return st;
+    st = make_q_map(&q_map, q, batch);
+    if (st != DSA_OK) return st;
+    dsa::ScoresParams p{};
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.w = w;
+    p.out = out;
+    p.err = static_cast<uint32_t*>(workspace);
+    p.num_pages = num_pages;
+    p.max_context = max_context;
+    p.row_width = max_context / 4;
+    p.table_width = int32_t(max_context / DSA_PAGE_TOKENS);
+    p.batch = batch;
+    p.fill_dead = fill_dead;
+    const cudaError_t e = dsa::launch_scores(keys_map, q_map, p, stream);
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "scores kernel launch");
+}
+
+dsa_status_t run_topk(const float* scores, const int32_t* seq_lens, int32_t batch, int64_t max_context, int32_t k,
+                      int32_t* topk_idx, void* workspace, cudaStream_t stream) {
+    dsa::TopkParams p{};
+    p.scores = scores;
+    p.seq_lens = seq_lens;
+    p.out = topk_idx;
+    p.err = static_cast<uint32_t*>(workspace);
+    p.max_context = max_context;
+    p.row_width = max_context / 4;
+    p.batch = batch;
+    p.k = k;
+    const cudaError_t e = dsa::launch_topk(p, stream);
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "top-k kernel launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dsa_indexer_workspace_size(int32_t batch, int64_t max_context, int32_t k) {
+    (void)k;
+    if (check_shape(batch, max_context) != DSA_OK) return 0;
+    return dsa::kWorkspaceHeaderBytes + size_t(batch) * size_t(max_context / 4) * sizeof(float);
+}
+
+dsa_status_t dsa_indexer_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+    if (check_workspace(workspace, workspace_bytes, dsa::kWorkspaceHeaderBytes) != DSA_OK) return DSA_ERR_WORKSPACE;
+    const cudaError_t e =
+        cudaMemsetAsync(workspace, 0, dsa::kWorkspaceHeaderBytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "workspace init");
+}
+
+dsa_status_t dsa_indexer_scores(const void* q, const float* w, const void* key_pool, int64_t num_pages,
+                                const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                                int64_t max_context, float* scores, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    dsa_status_t st = check_shape(batch, max_context);
+    if (st != DSA_OK) return st;
+    st = check_score_inputs(q, w, key_pool, num_pages, page_table, seq_lens);
+    if (st != DSA_OK) return st;
+    if (!scores || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
+    st = check_workspace(workspace, workspace_bytes, dsa::kWorkspaceHeaderBytes);
+    if (st != DSA_OK) return st;
+    return run_scores(q, w, key_pool, num_pages, page_table, seq_lens, batch, max_context, scores, 1, workspace,
+                      static_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_indexer_topk(const float* scores, const int32_t* seq_lens, int32_t batch, int64_t max_context,
+                              int32_t k, int32_t* topk_idx, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    dsa_status_t st = check_shape(batch, max_context);
+    if (st != DSA_OK) return st;
+    if (!scores || !seq_lens || !topk_idx || !aligned(scores, 4) || !aligned(seq_lens, 4) || !aligned(topk_idx, 4))
+        return DSA_ERR_INVALID_ARG;
+    if (k < 1 || int64_t(k) > max_context / 4) return DSA_ERR_INVALID_ARG;
+    st = check_workspace(workspace, workspace_bytes, dsa::kWorkspaceHeaderBytes);
+    if (st != DSA_OK) return st;
+    return run_topk(scores, seq_lens, batch, max_context, k, topk_idx, workspace, static_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_indexer_fused(const void* q, const float* w, const void* key_pool, int64_t num_pages,
+                               const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                               int64_t max_context, int32_t k, int32_t* topk_idx, float* scores_opt,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    dsa_status_t st = check_shape(batch, max_context);
+    if (st != DSA_OK) return st;
+    st = check_score_inputs(q, w, key_pool, num_pages, page_table, seq_lens);
+    if (st != DSA_OK) return st;
+    if (!topk_idx || !aligned(topk_idx, 4)) return DSA_ERR_INVALID_ARG;
+    if (scores_opt && !aligned(scores_opt, 16)) return DSA_ERR_INVALID_ARG;
+    if (k < 1 || int64_t(k) > max_context / 4) return DSA_ERR_INVALID_ARG;
+    const size_t need = scores_opt ? dsa::kWorkspaceHeaderBytes : dsa_indexer_workspace_size(batch, max_context, k);
+    st = check_workspace(workspace, workspace_bytes, need);
+    if (st != DSA_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* rows = scores_opt ? scores_opt
+                             : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kWorkspaceHeaderBytes);
+    st = run_scores(q, w, key_pool, num_pages, page_table, seq_lens, batch, max_context, rows, scores_opt ? 1 : 0,
+                    workspace, s);
+    if (st != DSA_OK) return st;
+    return run_topk(rows, seq_lens, batch, max_context, k, topk_idx, workspace, s);
+}
+
+dsa_status_t dsa_indexer_get_error(void* workspace, uint32_t* code, int clear, void* stream) {
+    if (!workspace || !code || !aligned(workspace, 256)) return DSA_ERR_INVALID_ARG;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && clear) e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "read error word");
+    *code = v;
+    return DSA_OK;
+}
+
+const char* dsa_status_string(dsa_status_t status) {
+    switch (status) {
+        case DSA_OK: return "ok";
+        case DSA_ERR_INVALID_ARG: return "invalid argument";
+        case DSA_ERR_UNSUPPORTED: return "unsupported shape";
+        case DSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case DSA_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+const char* dsa_indexer_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// indexer_kernels.h -- host-side launch interface of the indexer kernels
+// (internal to the library; the public ABI is include/dsa_indexer.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace dsa {
+
+// Fixed problem geometry.
+constexpr int kHeads = 32;
+constexpr int kHeadDim = 64;
+constexpr int kPageEntries = 64;                          // C4 keys per page
+constexpr int kPageBytes = kPageEntries * kHeadDim * 2;   // 8 KiB of bf16
+constexpr int kQRowBytes = kHeads * kHeadDim * 2;         // 4 KiB of bf16
+constexpr int kUnitPositions = 2 * kPageEntries;          // one work unit = 2 pages = 128 keys
+constexpr int kMaxBatch = 1024;
+constexpr size_t kWorkspaceHeaderBytes = 256;
+
+// Device error bits (same values as DSA_DEVERR_* in the public header).
+constexpr uint32_t kErrSeqLenClamped = 0x1u;
+constexpr uint32_t kErrBadPage = 0x2u;
+constexpr uint32_t kErrWaitTimeout = 0x4u;
+
+struct ScoresParams {
+    const int32_t* page_table;  // [batch, table_width]
+    const int32_t* seq_lens;    // [batch]
+    const float* w;             // [batch, 32]
+    float* out;                 // [batch, row_width]
+    uint32_t* err;              // device error word
+    int64_t num_pages;
+    int64_t max_context;        // tokens
+    int64_t row_width;          // max_context / 4
+    int32_t table_width;        // max_context / 256
+    int32_t batch;
+    int32_t fill_dead;          // 1: write -inf from the live extent to the row end
+};
+
+struct TopkParams {
+    const float* scores;  // [batch, row_width]
+    const int32_t* seq_lens;
+    int32_t* out;         // [batch, k]
+    uint32_t* err;
+    int64_t max_context;
+    int64_t row_width;
+    int32_t batch;
+    int32_t k;
+};
+
+// Scores kernel: persistent, one CTA per SM, TMA page gather + tcgen05 QK.
+cudaError_t launch_scores(const CUtensorMap& keys_map, const CUtensorMap& q_map, const ScoresParams& p,
+                          cudaStream_t stream);
+
+// Top-k kernel: one CTA per request row, radix select over live positions.
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
+
+}  // namespace dsa
