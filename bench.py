@@ -300,6 +300,52 @@ def run_ours(args):
         raise RuntimeError("device error word set during the timed steps")
 
     # e2e: host (pinned) inputs -> device, both calls, top-k back to the host, every step.
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(args, case, binding, scores, topk, ws, device, stream, world, live)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, args.cpu_sample_rows)
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    peak, peak_kind = measured_hbm_peak()
+    mean_scores = statistics.fmean(t_scores)
+    achieved = live * KEY_BYTES_PER_POSITION / mean_scores / 1e9
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.fmean(t_step), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(case, world),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": "scores_kernel",
+                     "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
+                     "algorithmic_bytes_per_launch": live * KEY_BYTES_PER_POSITION},
+        "kernels_us": {"scores_mean": 1e6 * mean_scores, "scores_median": 1e6 * statistics.median(t_scores),
+                       "topk_mean": 1e6 * statistics.fmean(t_topk),
+                       "step_p10": 1e6 * float(np.percentile(t_step, 10)),
+                       "step_p50": 1e6 * float(np.percentile(t_step, 50)),
+                       "step_p90": 1e6 * float(np.percentile(t_step, 90))},
+        "step_gbs_live_keys": live * KEY_BYTES_PER_POSITION / statistics.fmean(t_step) / 1e9,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * n * world,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": wall1 - wall0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(args, case, binding, scores, topk, ws, device, stream, world, live):
+    """Same step through the C ABI with host buffers: H2D of every input, D2H of the top-k."""
+    import torch
+    import torch.distributed as dist
+    B, K = case.batch, case.k
     host = [torch.from_numpy(a).pin_memory() for a in
             (case.q.view("int16"), case.w, case.key_pool.view("int16"), case.page_table, case.seq_lens)]
     dev_in = [torch.empty(h.shape, dtype=h.dtype, device=device) for h in host]
@@ -330,43 +376,8 @@ def run_ours(args):
     e2e_units, e2e_seconds = aggregate(live * args.e2e_steps, e0.elapsed_time(e1) * 1e-3)
     if not np.array_equal(out_host.numpy(), topk.cpu().numpy()):
         raise RuntimeError("e2e top-k read-back mismatch")
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(case, args.cpu_sample_rows)
-
-    if world > 1:
-        dist.destroy_process_group()
-    if rank != 0:
-        return 0
-
-    peak, peak_kind = measured_hbm_peak()
-    mean_scores = statistics.fmean(t_scores)
-    achieved = live * KEY_BYTES_PER_POSITION / mean_scores / 1e9
-    traffic = profiled_traffic()
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n, "warmup": args.warmup,
-        "ms_per_step": 1e3 * statistics.fmean(t_step), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(case, world),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "kernel": "scores_kernel",
-                     "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
-                     "algorithmic_bytes_per_launch": live * KEY_BYTES_PER_POSITION},
-        "kernels_us": {"scores_mean": 1e6 * mean_scores, "scores_median": 1e6 * statistics.median(t_scores),
-                       "topk_mean": 1e6 * statistics.fmean(t_topk),
-                       "step_p10": 1e6 * float(np.percentile(t_step, 10)),
-                       "step_p50": 1e6 * float(np.percentile(t_step, 50)),
-                       "step_p90": 1e6 * float(np.percentile(t_step, 90))},
-        "step_gbs_live_keys": live * KEY_BYTES_PER_POSITION / statistics.fmean(t_step) / 1e9,
-        "cpu_baseline": cpu,
-        "e2e": {"value": e2e_units / e2e_seconds, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * n * world,
-        "clocks": clocks.summary(),
-        "wall_s_timed_region": wall1 - wall0,
-    }
-    print(json.dumps(line), flush=True)
-    return 0
+    return {"value": e2e_units / e2e_seconds, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
 
 
 def main(argv=None):
