@@ -144,6 +144,29 @@ DSA_API dsa_status_t dsa_indexer_fused(const void *q, const float *w, const void
                                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * dsa_indexer_fused without a scores row and without a workspace argument,
+ * for callers that cannot allocate device memory on the path that runs the
+ * indexer (a serving engine that owns all of HBM and hands kernels only
+ * their tensors, custom-op hosts that provide no scratch, code that must not
+ * call cudaMalloc because it can synchronise the device).  The source pages
+ * have no counterpart to this entry point; it exists for those callers.
+ *
+ * Scratch: a library-owned device array of 256 B + 16 MiB, held by every GPU
+ * that loads the library until the process exits.  batch x max_context / 4
+ * fp32 live-score slots must fit in the 16 MiB, otherwise the call returns
+ * DSA_ERR_UNSUPPORTED and launches nothing.  The first call on a device looks
+ * up the array's device address (once per device) and must come before any
+ * stream capture on that device.  All calls share the array: calls that
+ * overlap on the GPU (unordered streams) race on it.  Each call clears the
+ * array's error word before it launches; device error bits are not reported
+ * by this entry point.  Same inputs and output as dsa_indexer_fused.
+ */
+DSA_API dsa_status_t dsa_indexer_fused_noalloc(const void *q, const float *w, const void *key_pool,
+                                       int64_t num_pages, const int32_t *page_table,
+                                       const int32_t *seq_lens, int32_t batch, int64_t max_context,
+                                       int32_t k, int32_t *topk_idx, void *stream);
+
+/*
  * Read the sticky device error word into *code (host pointer).  Synchronises
  * `stream` (not capture-safe).  clear != 0 zeroes the word afterwards.
  */
