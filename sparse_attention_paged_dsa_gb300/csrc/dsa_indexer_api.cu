@@ -180,7 +180,7 @@ dsa_status_t dsa_indexer_topk(const float* scores, const int32_t* seq_lens, int3
                               void* stream) {
     dsa_status_t st = check_shape(batch, max_context);
     if (st != DSA_OK) return st;
-    if (!scores || !seq_lens || !topk_idx || !aligned(scores, 4) || !aligned(seq_lens, 4) || !aligned(topk_idx, 4))
+    if (!scores || !seq_lens || !topk_idx || !aligned(scores, 16) || !aligned(seq_lens, 4) || !aligned(topk_idx, 4))
         return DSA_ERR_INVALID_ARG;
     if (k < 1 || int64_t(k) > max_context / 4) return DSA_ERR_INVALID_ARG;
     st = check_workspace(workspace, workspace_bytes, dsa::kWorkspaceHeaderBytes);

@@ -12,23 +12,34 @@
 // Blackwell", section "The Bottleneck That Was".
 //
 // Design (GB300-first, not the pages' one-program-per-page Triton kernel):
-//   * Persistent grid of one CTA per SM.  The grid size depends only on the
-//     device, so graph capture is safe; the work is split by live work units,
-//     so the cost is O(live positions), not O(max_context).
+//   * Persistent grid of kCtasPerSm CTAs per SM; its size depends only on the
+//     device, so graph capture is safe and a 1M-token max_context launches the
+//     same grid as an 8K one.
 //   * Work unit = 2 consecutive pages of one request = 128 keys = 16 KiB.
-//     Each CTA takes a contiguous range of the batch's live units.
-//   * Warp 0 (one lane) gathers pages with TMA tiled loads (128-byte swizzle)
-//     into an 8-stage shared-memory ring, plus the request's 4 KiB query
-//     tile; page ids for 32 units at a time are fetched by the whole warp so
-//     that the page-table latency is paid once per 32 units.
+//     Each CTA first takes an equal contiguous range holding 7/8 of the
+//     batch's live units (few request changes per CTA); the last 1/8 is
+//     handed out in small chunks from a counter in the workspace header, so
+//     that CTAs that draw slower memory take fewer of them and all finish
+//     together.  The last CTA to leave resets the counter.  Cost is O(live
+//     units), not O(max_context).
+//   * Warp 0 (one lane issues) gathers pages with TMA tiled loads (128-byte
+//     swizzle) into a kStages ring of 16 KiB stages; page ids (and the next
+//     chunk number) are fetched one batch ahead.  The request's 4 KiB query
+//     tile is loaded once per request change into a small ring of its own.
+//     Each unit's request, page pair and page validity go to a small
+//     metadata ring.
 //   * Warp 1 (one lane) issues tcgen05.mma kind::f16, M=128 keys x N=32 heads
-//     x K=64 dims (4 instructions of K=16), fp32 accumulators in TMEM, 4
-//     accumulator stages of 32 columns.
-//   * Warps 2-5 read the accumulators with tcgen05.ld (thread = key row,
-//     registers = 32 heads), apply relu, the head weights and the head sum in
-//     registers, mask, and store 128 contiguous fp32 scores per unit.  Before
-//     the unit loop they also stream -inf over the dead part of every row
-//     (split evenly over all CTAs) when a full-width row is requested.
+//     x K=64 dims (4 instructions of K=16) into one of 4 TMEM accumulators of
+//     32 fp32 columns, then publishes the accumulator and the unit's metadata.
+//   * kEpiGroups groups of 4 warps (group g takes every kEpiGroups-th unit)
+//     read the accumulators with tcgen05.ld (thread = key row, registers =
+//     32 heads), apply relu, the head weights and the head sum in registers,
+//     mask, and store 128 contiguous fp32 scores per unit.  Before that they
+//     stream -inf over the dead part of every row (split over all CTAs) when
+//     a full-width row is requested.
+//   * Programmatic dependent launch: barrier and TMEM set-up overlap the tail
+//     of the previous kernel; global memory is touched only after
+//     griddepcontrol.wait.
 //   * Every wait is bounded (about 1 s); a timeout sets an error bit, stops
 //     all roles, drains in-flight copies and MMAs and frees TMEM.
 #include <cuda.h>
@@ -39,33 +50,63 @@
 #include "indexer_kernels.h"
 #include "sm103_ptx.cuh"
 
+
 namespace dsa {
 namespace {
 
-constexpr int kStages = 8;
+constexpr int kStages = 4;                             // 16 KiB stages per CTA
+constexpr int kEpiGroups = 2;                          // epilogue groups of 4 warps
+constexpr int kCtasPerSm = 2;                          // two independent pipelines per SM
+constexpr int kChunk = 2;                              // units per dynamic scheduling step
+constexpr int kStaticEighths = 7;                      // share of the units assigned statically
+constexpr int kBatch = 32;                             // units prepared per warp-wide page-table load
+constexpr int kQSlots = 4;
 constexpr int kAccStages = 4;
-constexpr int kAccCols = 32;                         // fp32 columns per accumulator (N = 32 heads)
+constexpr int kMetaRing = 16;                          // >= kStages + kAccStages + 1
+constexpr int kAccCols = 32;                           // fp32 columns per accumulator (N = 32 heads)
 constexpr uint32_t kTmemCols = kAccStages * kAccCols;  // 128 (power of two >= 32)
-constexpr int kThreads = 192;                        // 6 warps
-constexpr int kATileBytes = 2 * kPageBytes;          // 16 KiB: 128 keys x 128 B
-constexpr int kStageBytes = kATileBytes + kQRowBytes;  // 20 KiB, multiple of 1024
+constexpr int kEpiThreads = 128 * kEpiGroups;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kStageBytes = 2 * kPageBytes;            // 16 KiB: 128 keys x 128 B
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kAccCols);
+constexpr int kEndOfWork = -1;                         // metadata marker: no more units
+static_assert(kAccStages % kEpiGroups == 0, "each epilogue group owns whole accumulator stages");
+static_assert(kMetaRing >= kStages + kAccStages + 1, "metadata ring too small");
+static_assert(kChunk >= 1 && kChunk <= kBatch, "a chunk is prepared by one warp");
+
+// Unit metadata: request (10 bits), page pair within the request (15 bits),
+// validity of its two pages (2 bits).  Max row width 2^22 C4 positions keeps
+// the pair below 2^15; kMaxBatch = 1024 keeps the request below 2^10.
+__device__ __forceinline__ int pack_meta(int b, int pair, bool ok0, bool ok1) {
+    return (b << 17) | (pair << 2) | (ok1 ? 2 : 0) | (ok0 ? 1 : 0);
+}
+__device__ __forceinline__ int meta_row(int m) { return m >> 17; }
+__device__ __forceinline__ int meta_pair(int m) { return (m >> 2) & 0x7FFF; }
+
+// Scheduling words in the 256-byte workspace header (word 0 is the error word).
+constexpr int kHeaderNextChunkWord = 32;  // byte 128
+constexpr int kHeaderExitWord = 48;       // byte 192
 
 struct __align__(8) SmemCtl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t qfull[kQSlots];
+    uint64_t qempty[kQSlots];
     uint64_t tfull[kAccStages];
     uint64_t tempty[kAccStages];
+    uint64_t tmeta[kAccStages];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
+    int32_t meta[kMetaRing];
     int32_t n_live[kMaxBatch];
     int32_t unit_start[kMaxBatch + 1];
 };
 
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + size_t(kStages) * kStageBytes + sizeof(SmemCtl);
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+constexpr size_t kTileBytes = size_t(kStages) * kStageBytes + size_t(kQSlots) * kQRowBytes;
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes + sizeof(SmemCtl);
+static_assert(kSmemBytes * kCtasPerSm <= 228 * 1024, "shared memory budget per SM");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget per CTA");
 
 // Largest b in [0, batch) with unit_start[b] <= u (rows without units share
 // their start with the next row, so this lands on the row that owns u).
@@ -81,26 +122,64 @@ __device__ __forceinline__ int row_of_unit(const int32_t* unit_start, int batch,
     return lo;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void wait_landed(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
+    }
+}
+
+// One lane's unit of a batch: its request, page pair and page ids (-2: no live second page).
+struct UnitPrep {
+    int b = 0;
+    int pair = 0;
+    int pg0 = -1;
+    int pg1 = -2;
+};
+
+// Lane l prepares unit u0 + l when l < cnt (page-table loads in flight on return).
+__device__ __forceinline__ UnitPrep prepare_units(const SmemCtl& ctl, const ScoresParams& p, int u0, int cnt,
+                                                  int lane) {
+    UnitPrep c;
+    if (lane < cnt) {
+        const int u = u0 + lane;
+        c.b = row_of_unit(ctl.unit_start, p.batch, u);
+        c.pair = u - ctl.unit_start[c.b];
+        const int live_pages = (ctl.n_live[c.b] + kPageEntries - 1) / kPageEntries;
+        const int32_t* row = p.page_table + int64_t(c.b) * p.table_width;
+        c.pg0 = __ldg(row + 2 * c.pair);
+        c.pg1 = (2 * c.pair + 1 < live_pages) ? __ldg(row + 2 * c.pair + 1) : -2;
+    }
+    return c;
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     scores_kernel(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CUtensorMap q_map,
                   const ScoresParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(tiles + size_t(kStages) * kStageBytes);
+    uint8_t* qtiles = tiles + size_t(kStages) * kStageBytes;
+    SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(tiles + kTileBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int batch = p.batch;
+    const int grid = gridDim.x;
 
-    // ---- set-up: barriers, TMEM, per-row live counts and unit prefix.
+    // ---- set-up that touches no global memory (overlaps the previous kernel).
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl.full[s], 1);
             mbar_init(&ctl.empty[s], 1);
         }
+        for (int s = 0; s < kQSlots; ++s) {
+            mbar_init(&ctl.qfull[s], 1);
+            mbar_init(&ctl.qempty[s], 1);
+        }
         for (int a = 0; a < kAccStages; ++a) {
             mbar_init(&ctl.tfull[a], 1);
-            mbar_init(&ctl.tempty[a], 4 * 32);
+            mbar_init(&ctl.tempty[a], 128);
+            mbar_init(&ctl.tmeta[a], 1);
         }
         mbar_init(&ctl.drain, 1);
         ctl.abort = 0;
@@ -112,9 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(&ctl.tmem_base, kTmemCols);
         tmem_relinquish();
     }
+    pdl_wait_prior_grid();
+    pdl_allow_next_grid();
+
+    // ---- per-row live counts and unit prefix.
     if (warp == 2) {
-        // 32 lanes scan the batch: lane l owns rows [l*per, (l+1)*per).
-        const int per = (batch + 31) / 32;
+        const int per = (batch + 31) / 32;  // lane l owns rows [l*per, (l+1)*per)
         const int b0 = min(lane * per, batch), b1 = min(b0 + per, batch);
         int units = 0;
         bool clamped = false;
@@ -145,51 +227,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
 
     const int total_units = ctl.unit_start[batch];
-    const int grid = gridDim.x;
-    const int u_begin = static_cast<int>((int64_t(total_units) * blockIdx.x) / grid);
-    const int u_end = static_cast<int>((int64_t(total_units) * (blockIdx.x + 1)) / grid);
     const uint32_t tmem_base = ctl.tmem_base;
     const int64_t M = p.row_width;
-    const int W = p.table_width;
+    uint32_t* next_chunk_word = p.err + kHeaderNextChunkWord;
 
     if (warp == 0) {
-        // ================= producer: page ids, then TMA gathers =================
+        // ================= producer: schedule, page ids, TMA gathers =================
         const uint64_t pol_keys = l2_policy_evict_first();
         const uint64_t pol_q = l2_policy_evict_last();
         int stage = 0;
         uint32_t phase = 0;
-        int issued = 0;
+        int issued = 0, q_issued = 0, q_row = -1, seq = 0;
         bool stop = false;
-        for (int u0 = u_begin; u0 < u_end && !stop; u0 += 32) {
-            const int cnt = min(32, u_end - u0);
-            int b = 0, pg0 = -1, pg1 = -2;
-            if (lane < cnt) {
-                const int u = u0 + lane;
-                b = row_of_unit(ctl.unit_start, batch, u);
-                const int pair = u - ctl.unit_start[b];
-                const int live_pages = (ctl.n_live[b] + kPageEntries - 1) / kPageEntries;
-                const int32_t* row = p.page_table + int64_t(b) * W;
-                pg0 = __ldg(row + 2 * pair);
-                pg1 = (2 * pair + 1 < live_pages) ? __ldg(row + 2 * pair + 1) : -2;  // -2: no live page
+
+        // Static share: [blockIdx.x * S, (blockIdx.x + 1) * S); dynamic share: [grid * S, total) in chunks.
+        const int S = static_cast<int>((int64_t(total_units) * kStaticEighths) / (8 * int64_t(grid)));
+        int sp = blockIdx.x * S;
+        const int se = sp + S;
+        const int dyn0 = grid * S;
+        int ticket = 0;  // dynamic chunk number requested one batch ahead (lane 0)
+        if (lane == 0) ticket = int(atomicAdd(next_chunk_word, 1u));
+        auto next_batch = [&](int& u0, int& cnt) {
+            if (sp < se) {
+                u0 = sp;
+                cnt = min(kBatch, se - sp);
+                sp += cnt;
+                return;
             }
-            for (int i = 0; i < cnt; ++i) {
-                const int bi = __shfl_sync(0xffffffffu, b, i);
-                const int g0 = __shfl_sync(0xffffffffu, pg0, i);
-                const int g1 = __shfl_sync(0xffffffffu, pg1, i);
+            const int t = __shfl_sync(0xffffffffu, ticket, 0);
+            u0 = dyn0 + t * kChunk;
+            cnt = u0 < total_units ? min(kChunk, total_units - u0) : 0;
+            if (lane == 0 && cnt > 0) ticket = int(atomicAdd(next_chunk_word, 1u));
+        };
+
+        int cur_u0, cur_cnt;
+        next_batch(cur_u0, cur_cnt);
+        UnitPrep cur = prepare_units(ctl, p, cur_u0, cur_cnt, lane);
+        while (cur_cnt > 0 && !stop) {
+            int nxt_u0, nxt_cnt;
+            next_batch(nxt_u0, nxt_cnt);
+            const UnitPrep nxt = prepare_units(ctl, p, nxt_u0, nxt_cnt, lane);  // loads in flight
+            for (int i = 0; i < cur_cnt; ++i) {
+                const int bi = __shfl_sync(0xffffffffu, cur.b, i);
+                const int pi = __shfl_sync(0xffffffffu, cur.pair, i);
+                const int g0 = __shfl_sync(0xffffffffu, cur.pg0, i);
+                const int g1 = __shfl_sync(0xffffffffu, cur.pg1, i);
                 int failed = 0;
                 if (lane == 0) {
-                    if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort)) {
-                        failed = 1;
-                    } else {
+                    if (bi != q_row) {  // new request: its query tile goes to the next q slot
+                        const int qs = q_issued % kQSlots;
+                        if (!mbar_wait(&ctl.qempty[qs], ((q_issued / kQSlots) & 1) ^ 1u, &ctl.abort)) {
+                            failed = 1;
+                        } else {
+                            mbar_arrive_expect_tx(&ctl.qfull[qs], kQRowBytes);
+                            tma_load_2d(qtiles + size_t(qs) * kQRowBytes, &q_map, &ctl.qfull[qs], 0, bi * kHeads,
+                                        pol_q);
+                            ++q_issued;
+                            q_row = bi;
+                        }
+                    }
+                    if (!failed && !mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort)) failed = 1;
+                    if (!failed) {
                         const bool ok0 = g0 >= 0 && g0 < p.num_pages;
                         const bool ok1 = g1 >= 0 && g1 < p.num_pages;
                         if (!ok0 || (g1 != -2 && !ok1)) atomicOr(p.err, kErrBadPage);
-                        const uint32_t bytes = kQRowBytes + (ok0 ? kPageBytes : 0) + (ok1 ? kPageBytes : 0);
+                        ctl.meta[seq % kMetaRing] = pack_meta(bi, pi, ok0, ok1);
+                        const uint32_t bytes = (ok0 ? kPageBytes : 0) + (ok1 ? kPageBytes : 0);
                         uint8_t* a = tiles + size_t(stage) * kStageBytes;
-                        mbar_arrive_expect_tx(&ctl.full[stage], bytes);
-                        if (ok0) tma_load_3d(a, &keys_map, &ctl.full[stage], 0, 0, g0, pol_keys);
-                        if (ok1) tma_load_3d(a + kPageBytes, &keys_map, &ctl.full[stage], 0, 0, g1, pol_keys);
-                        tma_load_2d(a + kATileBytes, &q_map, &ctl.full[stage], 0, bi * kHeads, pol_q);
+                        if (bytes != 0) {
+                            mbar_arrive_expect_tx(&ctl.full[stage], bytes);
+                            if (ok0) tma_load_3d(a, &keys_map, &ctl.full[stage], 0, 0, g0, pol_keys);
+                            if (ok1) tma_load_3d(a + kPageBytes, &keys_map, &ctl.full[stage], 0, 0, g1, pol_keys);
+                        } else {
+                            mbar_arrive(&ctl.full[stage]);  // nothing to load: the stage is full at once
+                        }
                         ++issued;
                     }
                 }
@@ -197,10 +308,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     stop = true;
                     break;
                 }
+                ++seq;
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
+            }
+            cur_u0 = nxt_u0;
+            cur_cnt = nxt_cnt;
+            cur = nxt;
+        }
+        // One end-of-work marker per epilogue group.
+        for (int g = 0; g < kEpiGroups && !stop; ++g) {
+            int failed = 0;
+            if (lane == 0) {
+                if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort)) {
+                    failed = 1;
+                } else {
+                    ctl.meta[seq % kMetaRing] = kEndOfWork;
+                    mbar_arrive(&ctl.full[stage]);
+                }
+            }
+            if (__shfl_sync(0xffffffffu, failed, 0)) stop = true;
+            ++seq;
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
             }
         }
         if (lane == 0 && stop) {
@@ -209,44 +342,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Let every copy this CTA issued land before the CTA may exit.
         if (lane == 0 && ctl.abort) {
-            const int outstanding = issued < kStages ? issued : kStages;
             int s = stage;
             uint32_t ph = phase;
-            for (int i = 0; i < outstanding; ++i) {
+            for (int i = 0; i < min(issued, kStages); ++i) {
                 if (s == 0) {
                     s = kStages - 1;
                     ph ^= 1u;
                 } else {
                     --s;
                 }
-                const uint32_t a = smem_u32(&ctl.full[s]);
-                const uint64_t t0 = global_timer_ns();
-                while (!mbar_try_wait(a, ph) && global_timer_ns() - t0 < kWaitLimitNs) {
-                }
+                wait_landed(&ctl.full[s], ph);
             }
+            for (int j = max(0, q_issued - kQSlots); j < q_issued; ++j)
+                wait_landed(&ctl.qfull[j % kQSlots], (j / kQSlots) & 1);
         }
     } else if (warp == 1) {
         // ================= MMA issuer (one lane) =================
         if (lane == 0) {
-            int stage = 0, acc = 0;
+            int stage = 0, acc = 0, seq = 0, ends = 0;
             uint32_t phase = 0, acc_phase = 0;
+            int q_row = -1, q_used = -1;
             bool stop = false;
-            for (int u = u_begin; u < u_end; ++u) {
-                if (!mbar_wait(&ctl.full[stage], phase, &ctl.abort) ||
-                    !mbar_wait(&ctl.tempty[acc], acc_phase ^ 1u, &ctl.abort)) {
+            while (true) {
+                bool ok = mbar_wait(&ctl.full[stage], phase, &ctl.abort);
+                ok = ok && mbar_wait(&ctl.tempty[acc], acc_phase ^ 1u, &ctl.abort);
+                if (!ok) {
                     stop = true;
                     break;
                 }
-                tc_fence_after_sync();
-                const uint32_t a_addr = smem_u32(tiles + size_t(stage) * kStageBytes);
-                const uint64_t a_desc = smem_desc_kmajor_sw128(a_addr);
-                const uint64_t b_desc = smem_desc_kmajor_sw128(a_addr + kATileBytes);
-                const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
+                const int m = ctl.meta[seq % kMetaRing];
+                if (m != kEndOfWork) {
+                    const int b = meta_row(m);
+                    if (b != q_row) {
+                        if (q_used >= 0) umma_commit(&ctl.qempty[q_used % kQSlots]);  // after the last MMA on it
+                        ++q_used;
+                        q_row = b;
+                        if (!mbar_wait(&ctl.qfull[q_used % kQSlots], (q_used / kQSlots) & 1, &ctl.abort)) {
+                            stop = true;
+                            break;
+                        }
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t a_desc = smem_desc_kmajor_sw128(smem_u32(tiles + size_t(stage) * kStageBytes));
+                    const uint64_t b_desc =
+                        smem_desc_kmajor_sw128(smem_u32(qtiles + size_t(q_used % kQSlots) * kQRowBytes));
+                    const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
 #pragma unroll
-                for (int kk = 0; kk < kHeadDim / 16; ++kk)  // K = 16 per MMA: +32 bytes = +2 in the address field
-                    umma_bf16_ss(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, kIdesc, kk > 0 ? 1u : 0u);
-                umma_commit(&ctl.empty[stage]);
-                umma_commit(&ctl.tfull[acc]);
+                    for (int kk = 0; kk < kHeadDim / 16; ++kk)  // K = 16 per MMA: +32 bytes = +2 in the address field
+                        umma_bf16_ss(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, kIdesc, kk > 0 ? 1u : 0u);
+                    umma_commit(&ctl.empty[stage]);
+                    umma_commit(&ctl.tfull[acc]);
+                }
+                mbar_arrive(&ctl.tmeta[acc]);  // the unit's metadata (or the end marker) is readable
+                ++seq;
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1u;
@@ -255,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc = 0;
                     acc_phase ^= 1u;
                 }
+                if (m == kEndOfWork && ++ends == kEpiGroups) break;
             }
             if (stop) {
                 atomicOr(p.err, kErrWaitTimeout);
@@ -262,95 +411,81 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Every MMA issued so far completes before TMEM is released.
             umma_commit(&ctl.drain);
-            const uint32_t a = smem_u32(&ctl.drain);
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(a, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
-            }
+            wait_landed(&ctl.drain, 0);
         }
         __syncwarp();
     } else {
-        // ================= epilogue: warps 2..5 =================
-        const int et = threadIdx.x - 64;   // 0..127
-        const int quad = warp & 3;         // TMEM lanes [32*quad, 32*quad + 32)
+        // ================= epilogue: kEpiGroups groups of 4 warps =================
+        const int et = threadIdx.x - 64;    // 0 .. kEpiThreads-1
+        const int group = (warp - 2) >> 2;  // takes the group-th, (group + kEpiGroups)-th, ... units
+        const int quad = warp & 3;          // TMEM lanes [32*quad, 32*quad + 32)
         const float neg_inf = __int_as_float(0xff800000);
 
         if (p.fill_dead) {
             const float4 ninf4 = make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
-            const int64_t stride = int64_t(grid) * 128;
+            const int64_t stride = int64_t(grid) * kEpiThreads;
             for (int b = 0; b < batch; ++b) {
                 const int64_t units = ctl.unit_start[b + 1] - ctl.unit_start[b];
                 const int64_t extent = units * kUnitPositions < M ? units * kUnitPositions : M;
                 float4* row = reinterpret_cast<float4*>(p.out + int64_t(b) * M);
-                for (int64_t i = extent / 4 + int64_t(blockIdx.x) * 128 + et; i < M / 4; i += stride)
+                for (int64_t i = extent / 4 + int64_t(blockIdx.x) * kEpiThreads + et; i < M / 4; i += stride)
                     __stcs(row + i, ninf4);
             }
         }
 
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        int cur_b = -1;
+        int cur_b = -1, n = 0;
         float wv[kHeads];
 #pragma unroll
         for (int h = 0; h < kHeads; ++h) wv[h] = 0.f;
         bool stop = false;
-        for (int u0 = u_begin; u0 < u_end && !stop; u0 += 32) {
-            const int cnt = min(32, u_end - u0);
-            int b = 0, pair = 0, pg = -2, n = 0;
-            if (lane < cnt) {
-                const int u = u0 + lane;
-                b = row_of_unit(ctl.unit_start, batch, u);
-                pair = u - ctl.unit_start[b];
+        for (int i = group;; i += kEpiGroups) {
+            const int acc = i % kAccStages;
+            const uint32_t acc_phase = uint32_t(i / kAccStages) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(&ctl.tmeta[acc], acc_phase, &ctl.abort))) {
+                stop = true;
+                break;
+            }
+            const int m = ctl.meta[i % kMetaRing];
+            if (m == kEndOfWork) break;
+            const int b = meta_row(m);
+            const int pair = meta_pair(m);
+            const bool page_ok = (m >> (quad >> 1)) & 1;  // quadrants 0-1: first page, 2-3: second
+            if (b != cur_b) {
+                const float4* wr = reinterpret_cast<const float4*>(p.w + int64_t(b) * kHeads);
+#pragma unroll
+                for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+                    const float4 v = __ldg(wr + h4);
+                    wv[4 * h4 + 0] = v.x;
+                    wv[4 * h4 + 1] = v.y;
+                    wv[4 * h4 + 2] = v.z;
+                    wv[4 * h4 + 3] = v.w;
+                }
                 n = ctl.n_live[b];
-                const int j = 2 * pair + (quad >> 1);  // page holding this warp's 32 keys
-                const int live_pages = (n + kPageEntries - 1) / kPageEntries;
-                pg = j < live_pages ? __ldg(p.page_table + int64_t(b) * W + j) : -2;
+                cur_b = b;
             }
-            for (int i = 0; i < cnt; ++i) {
-                const int bi = __shfl_sync(0xffffffffu, b, i);
-                const int pi = __shfl_sync(0xffffffffu, pair, i);
-                const int gi = __shfl_sync(0xffffffffu, pg, i);
-                const int ni = __shfl_sync(0xffffffffu, n, i);
-                if (bi != cur_b) {
-                    const float4* wr = reinterpret_cast<const float4*>(p.w + int64_t(bi) * kHeads);
-#pragma unroll
-                    for (int h4 = 0; h4 < kHeads / 4; ++h4) {
-                        const float4 v = __ldg(wr + h4);
-                        wv[4 * h4 + 0] = v.x;
-                        wv[4 * h4 + 1] = v.y;
-                        wv[4 * h4 + 2] = v.z;
-                        wv[4 * h4 + 3] = v.w;
-                    }
-                    cur_b = bi;
-                }
-                const bool ok = mbar_wait(&ctl.tfull[acc], acc_phase, &ctl.abort);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    stop = true;
-                    break;
-                }
-                tc_fence_after_sync();
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * kAccCols), r);
-                tmem_ld_wait(r);
-                tc_fence_before_sync();
-                mbar_arrive(&ctl.tempty[acc]);
+            const bool okf = mbar_wait(&ctl.tfull[acc], acc_phase, &ctl.abort);
+            if (!__all_sync(0xffffffffu, okf)) {
+                stop = true;
+                break;
+            }
+            tc_fence_after_sync();
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * kAccCols), r);
+            tmem_ld_wait(r);
+            tc_fence_before_sync();
+            mbar_arrive(&ctl.tempty[acc]);
 
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-                for (int h = 0; h < kHeads; h += 4) {
-                    s0 = fmaf(wv[h + 0], fmaxf(__uint_as_float(r[h + 0]), 0.f), s0);
-                    s1 = fmaf(wv[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
-                    s2 = fmaf(wv[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
-                    s3 = fmaf(wv[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
-                }
-                const float s = (s0 + s1) + (s2 + s3);
-                const int64_t t = int64_t(pi) * kUnitPositions + quad * 32 + lane;
-                const bool valid = t < ni && gi >= 0 && gi < p.num_pages;
-                if (t < M) p.out[int64_t(bi) * M + t] = valid ? s : neg_inf;
-                if (++acc == kAccStages) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
+            for (int h = 0; h < kHeads; h += 4) {
+                s0 = fmaf(wv[h + 0], fmaxf(__uint_as_float(r[h + 0]), 0.f), s0);
+                s1 = fmaf(wv[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
+                s2 = fmaf(wv[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
+                s3 = fmaf(wv[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
             }
+            const float s = (s0 + s1) + (s2 + s3);
+            const int64_t t = int64_t(pair) * kUnitPositions + quad * 32 + lane;
+            if (t < M) p.out[int64_t(b) * M + t] = (t < n && page_ok) ? s : neg_inf;
         }
         if (stop && lane == 0) {
             atomicOr(p.err, kErrWaitTimeout);
@@ -360,6 +495,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    if (threadIdx.x == 0) {
+        // The last CTA out resets the chunk counter for the next launch.
+        __threadfence();
+        if (atomicAdd(p.err + kHeaderExitWord, 1u) == uint32_t(grid - 1)) {
+            atomicExch(next_chunk_word, 0u);
+            atomicExch(p.err + kHeaderExitWord, 0u);
+        }
+    }
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, kTmemCols);
@@ -383,8 +526,17 @@ cudaError_t launch_scores(const CUtensorMap& keys_map, const CUtensorMap& q_map,
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    scores_kernel<<<sms, kThreads, kSmemBytes, stream>>>(keys_map, q_map, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(sms * kCtasPerSm));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, scores_kernel, keys_map, q_map, p);
 }
 
 }  // namespace dsa

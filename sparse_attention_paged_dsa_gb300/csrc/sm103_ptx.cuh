@@ -68,6 +68,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Block until the grid this launch depends on has completed and its memory
+// is visible (a no-op when launched without the programmatic attribute).
+__device__ __forceinline__ void pdl_wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next programmatic-dependent launch in the stream to be scheduled.
+__device__ __forceinline__ void pdl_allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- L2 hints
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;

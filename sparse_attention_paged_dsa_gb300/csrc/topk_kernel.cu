@@ -9,24 +9,33 @@
 //
 // Selection (exact, deterministic): scores are mapped to order-preserving
 // 32-bit keys; three histogram passes (11 + 11 + 10 bits) find the key T of
-// the k-th largest score and how many of the keys equal to T are taken; a
-// final ordered pass keeps every key > T and the first ones equal to T in
-// position order (equal scores: lower position wins), writing positions in
-// ascending order.  One 1024-thread CTA per request; rows of up to 49152 live
-// positions are held in shared memory between passes, longer rows are
-// re-read from global memory (L2) on each pass.
+// the k-th largest score and how many of the keys equal to T are taken (the
+// lowest positions); every key > T and those keys == T are written in
+// ascending position.  One 1024-thread CTA per request.
+//   * n_b <= 32768: each thread holds 32 consecutive keys in registers.  The
+//     row is read with coalesced 16-byte loads (all of a thread's loads issued
+//     before any is used) and transposed through padded shared memory; the
+//     histogram passes are register loops and the ordered output needs one
+//     block scan of per-thread counts.
+//   * longer rows: keys stay in shared memory (up to 49152) or are re-read
+//     from global memory (L2) on each pass, and the output is an ordered
+//     compaction over per-warp segments.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "indexer_kernels.h"
+#include "sm103_ptx.cuh"
 
 namespace dsa {
 namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCacheCap = 49152;  // keys held in shared memory (192 KiB)
+constexpr int kCacheCap = 49152;                    // keys held in shared memory (192 KiB)
+constexpr int kKeysPerThread = 32;                  // register path: keys per thread
+constexpr int kRegCap = kThreads * kKeysPerThread;  // 32768
+constexpr int kLoadsPerThread = kRegCap / 4 / kThreads;  // float4 loads per thread on the register path
 
 __device__ __forceinline__ uint32_t order_key(float x) {
     const uint32_t u = __float_as_uint(x);
@@ -86,6 +95,142 @@ __device__ __forceinline__ void select_bin(TopkSmem& sm, uint32_t kk) {
     __syncthreads();
 }
 
+__device__ __forceinline__ void clear_hist(TopkSmem& sm) {
+    for (int i = threadIdx.x; i < 2048; i += kThreads) sm.hist[i] = 0;
+}
+
+// Exclusive prefix over the block, in thread order, of two per-thread counts.
+__device__ __forceinline__ void block_scan2(TopkSmem& sm, uint32_t a, uint32_t b, uint32_t& a_before,
+                                            uint32_t& b_before) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t ai = a, bi = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, ai, o);
+        const uint32_t y = __shfl_up_sync(0xffffffffu, bi, o);
+        if (lane >= o) {
+            ai += x;
+            bi += y;
+        }
+    }
+    if (lane == 31) {
+        sm.warp_gt[warp] = ai;
+        sm.warp_eq[warp] = bi;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t g = sm.warp_gt[lane], e = sm.warp_eq[lane];
+        uint32_t gs = g, es = e;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(0xffffffffu, gs, o);
+            const uint32_t y = __shfl_up_sync(0xffffffffu, es, o);
+            if (lane >= o) {
+                gs += x;
+                es += y;
+            }
+        }
+        sm.warp_gt[lane] = gs - g;
+        sm.warp_eq[lane] = es - e;
+    }
+    __syncthreads();
+    a_before = sm.warp_gt[warp] + ai - a;
+    b_before = sm.warp_eq[warp] + bi - b;
+}
+
+// ------------------------------------------------------------ register path
+// Shared-memory slot of position p: one pad word after every 32 keys, so that
+// thread i reading its key j hits bank (i + j) % 32.
+__device__ __forceinline__ int pad_slot(int p) { return p + (p >> 5); }
+
+__device__ __forceinline__ void select_row_regs(TopkSmem& sm, uint32_t* stage, const float* __restrict__ row, int n,
+                                                int k, int32_t* __restrict__ out) {
+    const int tid = threadIdx.x;
+    clear_hist(sm);
+
+    // All of this thread's 16-byte loads first (lane-consecutive: coalesced), then keys to shared memory.
+    const int n4 = n >> 2;
+    const float4* row4 = reinterpret_cast<const float4*>(row);
+    float4 v[kLoadsPerThread];
+#pragma unroll
+    for (int j = 0; j < kLoadsPerThread; ++j) {
+        const int i = tid + j * kThreads;
+        v[j] = i < n4 ? __ldcg(row4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int tail = (4 * n4 + tid < n) ? 4 * n4 + tid : -1;  // at most 3 trailing scores
+    const float vt = tail >= 0 ? __ldcg(row + tail) : 0.f;
+#pragma unroll
+    for (int j = 0; j < kLoadsPerThread; ++j) {
+        const int i = tid + j * kThreads;
+        if (i < n4) {
+            const int p = 4 * i;
+            stage[pad_slot(p + 0)] = order_key(v[j].x);
+            stage[pad_slot(p + 1)] = order_key(v[j].y);
+            stage[pad_slot(p + 2)] = order_key(v[j].z);
+            stage[pad_slot(p + 3)] = order_key(v[j].w);
+        }
+    }
+    if (tail >= 0) stage[pad_slot(tail)] = order_key(vt);
+    __syncthreads();
+
+    const int base = tid * kKeysPerThread;  // this thread's positions [base, base + 32)
+    const int valid = max(0, min(kKeysPerThread, n - base));
+    uint32_t key[kKeysPerThread];
+#pragma unroll
+    for (int j = 0; j < kKeysPerThread; ++j) key[j] = j < valid ? stage[pad_slot(base + j)] : 0u;
+
+#pragma unroll
+    for (int j = 0; j < kKeysPerThread; ++j)
+        if (j < valid) atomicAdd(&sm.hist[key[j] >> 21], 1u);
+    __syncthreads();
+    select_bin<2048>(sm, uint32_t(k));
+    const uint32_t bin1 = sm.result[0];
+    uint32_t kk = sm.result[1];
+
+    clear_hist(sm);
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kKeysPerThread; ++j)
+        if (j < valid && (key[j] >> 21) == bin1) atomicAdd(&sm.hist[(key[j] >> 10) & 0x7FFu], 1u);
+    __syncthreads();
+    select_bin<2048>(sm, kk);
+    const uint32_t prefix22 = (bin1 << 11) | sm.result[0];
+    kk = sm.result[1];
+
+    clear_hist(sm);
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kKeysPerThread; ++j)
+        if (j < valid && (key[j] >> 10) == prefix22) atomicAdd(&sm.hist[key[j] & 0x3FFu], 1u);
+    __syncthreads();
+    select_bin<1024>(sm, kk);
+    const uint32_t T = (prefix22 << 10) | sm.result[0];
+    const uint32_t take_eq = sm.result[1];
+
+    uint32_t gt = 0, eq = 0;
+#pragma unroll
+    for (int j = 0; j < kKeysPerThread; ++j) {
+        gt += (j < valid && key[j] > T) ? 1u : 0u;
+        eq += (j < valid && key[j] == T) ? 1u : 0u;
+    }
+    uint32_t gt_run, eq_run;  // keys > T and == T at lower positions
+    block_scan2(sm, gt, eq, gt_run, eq_run);
+#pragma unroll
+    for (int j = 0; j < kKeysPerThread; ++j) {
+        if (j < valid) {
+            if (key[j] > T) {
+                out[gt_run + min(eq_run, take_eq)] = base + j;
+                ++gt_run;
+            } else if (key[j] == T) {
+                if (eq_run < take_eq) out[gt_run + eq_run] = base + j;
+                ++eq_run;
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------- long-row path
 template <bool kCached>
 __device__ __forceinline__ uint32_t key_at(const uint32_t* cache, const float* row, int t) {
     if constexpr (kCached)
@@ -95,16 +240,29 @@ __device__ __forceinline__ uint32_t key_at(const uint32_t* cache, const float* r
 }
 
 template <bool kCached>
-__device__ void select_row(TopkSmem& sm, uint32_t* cache, const float* row, int n, int k, int32_t* out) {
+__device__ __forceinline__ void select_row(TopkSmem& sm, uint32_t* cache, const float* __restrict__ row, int n,
+                                           int k, int32_t* __restrict__ out) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    // Pass 1: top 11 bits of every live key (and fill the cache).
-    for (int i = tid; i < 2048; i += kThreads) sm.hist[i] = 0;
+    // Pass 1: top 11 bits of every live key (and fill the cache); 8 loads in flight per thread.
+    clear_hist(sm);
     __syncthreads();
-    for (int t = tid; t < n; t += kThreads) {
-        const uint32_t key = order_key(__ldcg(row + t));
-        if constexpr (kCached) cache[t] = key;
-        atomicAdd(&sm.hist[key >> 21], 1u);
+    for (int t0 = 0; t0 < n; t0 += 8 * kThreads) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int t = t0 + j * kThreads + tid;
+            v[j] = t < n ? __ldcg(row + t) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int t = t0 + j * kThreads + tid;
+            if (t < n) {
+                const uint32_t key = order_key(v[j]);
+                if constexpr (kCached) cache[t] = key;
+                atomicAdd(&sm.hist[key >> 21], 1u);
+            }
+        }
     }
     __syncthreads();
     select_bin<2048>(sm, uint32_t(k));
@@ -112,7 +270,7 @@ __device__ void select_row(TopkSmem& sm, uint32_t* cache, const float* row, int 
     uint32_t kk = sm.result[1];
 
     // Pass 2: next 11 bits among keys of bin1.
-    for (int i = tid; i < 2048; i += kThreads) sm.hist[i] = 0;
+    clear_hist(sm);
     __syncthreads();
     for (int t = tid; t < n; t += kThreads) {
         const uint32_t key = key_at<kCached>(cache, row, t);
@@ -124,7 +282,7 @@ __device__ void select_row(TopkSmem& sm, uint32_t* cache, const float* row, int 
     kk = sm.result[1];
 
     // Pass 3: last 10 bits among keys sharing the top 22 bits.
-    for (int i = tid; i < 1024; i += kThreads) sm.hist[i] = 0;
+    clear_hist(sm);
     __syncthreads();
     for (int t = tid; t < n; t += kThreads) {
         const uint32_t key = key_at<kCached>(cache, row, t);
@@ -191,6 +349,10 @@ __device__ void select_row(TopkSmem& sm, uint32_t* cache, const float* row, int 
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, int cache_cap) {
     extern __shared__ uint32_t cache[];
     __shared__ TopkSmem sm;
+    // Launched as a programmatic dependent of the scores kernel: wait for its
+    // results before touching global memory.
+    pdl_wait_prior_grid();
+    pdl_allow_next_grid();
     const int b = blockIdx.x;
     int64_t s = p.seq_lens[b];
     s = s < 0 ? 0 : (s > p.max_context ? p.max_context : s);
@@ -202,7 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
         return;
     }
     const float* row = p.scores + int64_t(b) * p.row_width;
-    if (n <= cache_cap)
+    if (n <= kRegCap && pad_slot(n) <= cache_cap)
+        select_row_regs(sm, cache, row, n, k, out);
+    else if (n <= cache_cap)
         select_row<true>(sm, cache, row, n, k, out);
     else
         select_row<false>(sm, cache, row, n, k, out);
@@ -211,8 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
 }  // namespace
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
-    const int64_t cap64 = p.row_width < kCacheCap ? p.row_width : kCacheCap;
-    const int cache_cap = p.row_width > p.k ? int(cap64) : 0;
+    // Shared keys: the row (padded by one word per 32 for the register path), capped at kCacheCap.
+    const int64_t want = p.row_width + p.row_width / 32 + 1;
+    const int cache_cap = p.row_width > p.k ? int(want < kCacheCap ? want : kCacheCap) : 0;
     const size_t smem = size_t(cache_cap) * sizeof(uint32_t);
     static bool configured[64] = {};
     int dev = 0;
@@ -225,8 +390,17 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    topk_kernel<<<p.batch, kThreads, smem, stream>>>(p, cache_cap);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(p.batch));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_kernel, p, cache_cap);
 }
 
 }  // namespace dsa
