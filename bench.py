@@ -55,6 +55,7 @@ def parse_args(argv=None):
                     help="rows of the workload the CPU baseline times (about 10-30 s on one core)")
     ap.add_argument("--reference-rows-per-step", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-context-scaling", action="store_true")
     return ap.parse_args(argv)
 
 
@@ -188,6 +189,56 @@ def cpu_baseline(case, rows: int):
                       f"{dt:.2f} s"}
 
 
+def graph_us_per_call(fn, reps=20, replays=20):
+    """GPU time per call of `fn`: `reps` calls captured in one CUDA graph and replayed (no host launch cost)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) * 1e3 / reps for a, b in times)
+
+
+def context_scaling(binding, inputs, device):
+    """Fused indexer without the full-width row on 64 requests of 512 tokens: max_context 1M vs 8K.
+
+    The same requests (same keys, same page ids) are scored with a page table 4096 pages wide and
+    one 32 pages wide; the ratio of GPU times is the cost of the larger fixed capture shape.
+    """
+    import torch
+    big = inputs.workload("b64_ctx1m_seq512")
+    small = inputs.IndexerCase("b64_ctx8k_seq512", big.q, big.w, big.key_pool,
+                               big.page_table[:, :8192 // inputs.PAGE_TOKENS].copy(), big.seq_lens, 8192, big.k)
+    out = {}
+    for label, c in (("1m", big), ("8k", small)):
+        q, w, pool, table, seq = binding.to_device(c, device)
+        ws = binding.new_workspace(c.batch, c.max_context, c.k, device)
+        topk = torch.empty((c.batch, c.k), dtype=torch.int32, device=device)
+        out[label] = graph_us_per_call(lambda: binding.dsa_indexer_fused(q, w, pool, table, seq, c.max_context, c.k,
+                                                                         topk_idx=topk, workspace=ws))
+        if binding.get_error(ws) != 0:
+            raise RuntimeError("device error word set in the context-scaling run")
+    return {"t_fused_no_row_1m_us": out["1m"], "t_fused_no_row_8k_us": out["8k"],
+            "ratio_1m_over_8k": out["1m"] / out["8k"],
+            "workload": "64 requests x 512 tokens, k=2048, same keys and page ids; CUDA-graph replay"}
+
+
 def workload_config(case, world):
     live = int(case.live_positions().sum())
     return {"workload": case.name, "batch": case.batch, "max_context": case.max_context,
@@ -318,6 +369,8 @@ def run_ours(args):
     if args.e2e_steps > 0:
         e2e = run_e2e(args, case, binding, scores, topk, ws, device, stream, world, live)
 
+    scaling_1m = context_scaling(binding, inputs, device) if not args.no_context_scaling else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(case, args.cpu_sample_rows)
@@ -346,6 +399,7 @@ def run_ours(args):
                        "step_p90": 1e6 * float(np.percentile(t_step, 90))},
         "step_gbs_live_keys": live * KEY_BYTES_PER_POSITION / statistics.fmean(t_step) / 1e9,
         "cpu_baseline": cpu,
+        "context_scaling": scaling_1m,
         "e2e": e2e,
         "gpu_launches": 2 * n * world,
         "step": "dsa_indexer_fused with the full-width scores row (scores kernel, then top-k kernel)",
