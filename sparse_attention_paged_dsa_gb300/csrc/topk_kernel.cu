@@ -7,16 +7,20 @@
 // This kernel only ever looks at positions t < n_b, so its cost is
 // O(live positions), and it does nothing but write indices when n_b <= k.
 //
-// Selection (exact, deterministic): scores are mapped to order-preserving
-// 32-bit keys; three histogram passes (11 + 11 + 10 bits) find the key T of
-// the k-th largest score and how many of the keys equal to T are taken (the
-// lowest positions); every key > T and those keys == T are written in
-// ascending position.  One 1024-thread CTA per request.
-//   * n_b <= 32768: each thread holds 32 consecutive keys in registers.  The
-//     row is read with coalesced 16-byte loads (all of a thread's loads issued
-//     before any is used) and transposed through padded shared memory; the
-//     histogram passes are register loops and the ordered output needs one
-//     block scan of per-thread counts.
+// Selection is exact and deterministic: scores are mapped to order-preserving
+// 32-bit keys; radix histograms (11 + 11 + 10 bits) find the key T of the
+// k-th largest score and how many keys equal to T are taken (the lowest
+// positions); every key > T and those keys == T are written in ascending
+// position.  One 1024-thread CTA per request.
+//   * n_b <= 32768, first choice (sampled path): keys stay in registers in
+//     load order; a histogram of every 4th key gives a threshold that keeps a
+//     little more than k keys; those are compacted, in position order, into a
+//     short list in shared memory, and the radix passes and the ordered write
+//     run on that list only.
+//   * n_b <= 32768 when the sample misjudges (fewer than k or too many keys
+//     pass): each thread holds 32 consecutive keys (transposed through padded
+//     shared memory); the radix passes run over all keys in registers and
+//     one block scan orders the output.
 //   * longer rows: keys stay in shared memory (up to 49152) or are re-read
 //     from global memory (L2) on each pass, and the output is an ordered
 //     compaction over per-warp segments.
@@ -48,20 +52,23 @@ struct TopkSmem {
     uint32_t warp_gt[kWarps];
     uint32_t warp_eq[kWarps];
     uint32_t result[2];
+    uint32_t hist2[2048];                        // second histogram buffer (list pass 2)
+    uint32_t chunk_tot[kLoadsPerThread];         // candidates per 4096-position chunk
+    uint32_t wpre[kLoadsPerThread][kWarps];      // candidates per (chunk, warp), then their prefix in the chunk
 };
 
 // Find the bin holding the kk-th largest key: result[0] = bin,
 // result[1] = how many keys of that bin are still to be taken.  Ends with a
 // barrier, so result[] is visible to all threads on return.
 template <int kBins>
-__device__ __forceinline__ void select_bin(TopkSmem& sm, uint32_t kk) {
+__device__ __forceinline__ void select_bin_from(TopkSmem& sm, const uint32_t* hist, uint32_t kk) {
     constexpr int per = kBins / kThreads;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t h[per];
     uint32_t v = 0;
 #pragma unroll
     for (int i = 0; i < per; ++i) {
-        h[i] = sm.hist[tid * per + i];
+        h[i] = hist[tid * per + i];
         v += h[i];
     }
     uint32_t incl = v;  // sum over this and higher lanes (higher bins)
@@ -93,6 +100,11 @@ __device__ __forceinline__ void select_bin(TopkSmem& sm, uint32_t kk) {
         above += h[i];
     }
     __syncthreads();
+}
+
+template <int kBins>
+__device__ __forceinline__ void select_bin(TopkSmem& sm, uint32_t kk) {
+    select_bin_from<kBins>(sm, sm.hist, kk);
 }
 
 __device__ __forceinline__ void clear_hist(TopkSmem& sm) {
@@ -230,6 +242,178 @@ __device__ __forceinline__ void select_row_regs(TopkSmem& sm, uint32_t* stage, c
     __syncthreads();
 }
 
+// ------------------------------------------------------------ sampled path
+// Rows of up to 32768 live positions.  Keys stay in registers in load order
+// (thread t holds positions 4 (t + 1024 j) + c).  Every 4th position is a
+// sample; the bin of the sample histogram that holds rank r (the expected
+// rank of the k-th largest among the samples plus four standard deviations)
+// gives a threshold tau that all but rarely keeps at least k keys.  Keys >= tau
+// are compacted in position order into shared memory, the exact 3-pass radix
+// select runs on that short list, and the output is an ordered filter of it.
+// Returns false, with nothing written, when fewer than k or more keys than the
+// list holds pass tau; the caller then runs the exact full-row path.
+__device__ __forceinline__ bool select_row_sampled(TopkSmem& sm, uint32_t* buf, int buf_words,
+                                                   const float* __restrict__ row, int n, int k,
+                                                   int32_t* __restrict__ out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kChunks = kLoadsPerThread;
+    clear_hist(sm);
+
+    uint32_t key[kKeysPerThread];  // key[4 j + c]: position 4 (tid + kThreads j) + c
+    const int n4 = n >> 2;
+    const float4* row4 = reinterpret_cast<const float4*>(row);
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+        const int i = tid + j * kThreads;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < n4) {
+            v = __ldcg(row4 + i);
+        } else if (i == n4) {  // the last, partial group of four
+            const int r = n - 4 * n4;
+            if (r > 0) v.x = __ldcg(row + 4 * i);
+            if (r > 1) v.y = __ldcg(row + 4 * i + 1);
+            if (r > 2) v.z = __ldcg(row + 4 * i + 2);
+        }
+        key[4 * j + 0] = order_key(v.x);
+        key[4 * j + 1] = order_key(v.y);
+        key[4 * j + 2] = order_key(v.z);
+        key[4 * j + 3] = order_key(v.w);
+    }
+    __syncthreads();  // histogram cleared
+
+    // Sample histogram: positions 4 i (the first key of each group of four).
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j)
+        if (4 * (tid + j * kThreads) < n) atomicAdd(&sm.hist[key[4 * j] >> 21], 1u);
+    __syncthreads();
+    const int ns = (n + 3) >> 2;
+    const float expect = float(k) * float(ns) / float(n);
+    const int r = min(ns, int(expect + 4.f * sqrtf(expect)) + 8);
+    select_bin<2048>(sm, uint32_t(r));
+    const uint32_t tau = sm.result[0] << 21;
+
+    // Candidates per chunk, ordered prefix over (chunk, warp, lane, c).
+    uint32_t lo = 0, hi = 0;  // 8-bit counts of chunks 0-3 and 4-7
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) c += (4 * (tid + j * kThreads) + q < n && key[4 * j + q] >= tau) ? 1u : 0u;
+        if (j < 4)
+            lo |= c << (8 * j);
+        else
+            hi |= c << (8 * (j - 4));
+    }
+    uint32_t lo_in = lo, hi_in = hi;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, lo_in, o);
+        const uint32_t y = __shfl_up_sync(0xffffffffu, hi_in, o);
+        if (lane >= o) {
+            lo_in += x;
+            hi_in += y;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j)
+            sm.wpre[j][warp] = ((j < 4 ? lo_in : hi_in) >> (8 * (j & 3))) & 0xFFu;
+    }
+    __syncthreads();
+    if (warp < kChunks) {  // warp j: exclusive prefix over the warps of chunk j
+        const uint32_t v = sm.wpre[warp][lane];
+        uint32_t s = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += x;
+        }
+        sm.wpre[warp][lane] = s - v;
+        if (lane == 31) sm.chunk_tot[warp] = s;
+    }
+    __syncthreads();
+    uint32_t total = 0;
+    uint32_t chunk_off[kChunks];
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+        chunk_off[j] = total;
+        total += sm.chunk_tot[j];
+    }
+    const int cap = min(16384, buf_words / 2);
+    if (total < uint32_t(k) || total > uint32_t(cap)) return false;
+
+    uint32_t* cand_key = buf;
+    uint32_t* cand_pos = buf + cap;
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+        const uint32_t incl = ((j < 4 ? lo_in : hi_in) >> (8 * (j & 3))) & 0xFFu;
+        const uint32_t own = ((j < 4 ? lo : hi) >> (8 * (j & 3))) & 0xFFu;
+        uint32_t slot = chunk_off[j] + sm.wpre[j][warp] + incl - own;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int pos = 4 * (tid + j * kThreads) + q;
+            if (pos < n && key[4 * j + q] >= tau) {
+                cand_key[slot] = key[4 * j + q];
+                cand_pos[slot] = uint32_t(pos);
+                ++slot;
+            }
+        }
+    }
+    const int C = int(total);
+
+    // Exact selection on the list (already in position order).  Pass 1 uses hist, pass 2 hist2
+    // (cleared with hist), pass 3 hist again.
+    clear_hist(sm);
+    for (int i = tid; i < 2048; i += kThreads) sm.hist2[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < C; i += kThreads) atomicAdd(&sm.hist[cand_key[i] >> 21], 1u);
+    __syncthreads();
+    select_bin<2048>(sm, uint32_t(k));
+    const uint32_t bin1 = sm.result[0];
+    uint32_t kk = sm.result[1];
+    for (int i = tid; i < C; i += kThreads) {
+        const uint32_t ck = cand_key[i];
+        if ((ck >> 21) == bin1) atomicAdd(&sm.hist2[(ck >> 10) & 0x7FFu], 1u);
+    }
+    __syncthreads();
+    select_bin_from<2048>(sm, sm.hist2, kk);
+    const uint32_t prefix22 = (bin1 << 11) | sm.result[0];
+    kk = sm.result[1];
+    clear_hist(sm);  // nobody reads pass 1's histogram any more
+    __syncthreads();
+    for (int i = tid; i < C; i += kThreads) {
+        const uint32_t ck = cand_key[i];
+        if ((ck >> 10) == prefix22) atomicAdd(&sm.hist[ck & 0x3FFu], 1u);
+    }
+    __syncthreads();
+    select_bin<1024>(sm, kk);
+    const uint32_t T = (prefix22 << 10) | sm.result[0];
+    const uint32_t take_eq = sm.result[1];
+
+    // Ordered filter: thread t owns list entries [t * per, t * per + per).
+    const int per = (C + kThreads - 1) / kThreads;
+    const int i0 = min(C, tid * per), i1 = min(C, i0 + per);
+    uint32_t gt = 0, eq = 0;
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t ck = cand_key[i];
+        gt += ck > T ? 1u : 0u;
+        eq += ck == T ? 1u : 0u;
+    }
+    uint32_t gt_run, eq_run;
+    block_scan2(sm, gt, eq, gt_run, eq_run);
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t ck = cand_key[i];
+        if (ck > T) {
+            out[gt_run + min(eq_run, take_eq)] = int32_t(cand_pos[i]);
+            ++gt_run;
+        } else if (ck == T) {
+            if (eq_run < take_eq) out[gt_run + eq_run] = int32_t(cand_pos[i]);
+            ++eq_run;
+        }
+    }
+    return true;
+}
+
 // ------------------------------------------------------- long-row path
 template <bool kCached>
 __device__ __forceinline__ uint32_t key_at(const uint32_t* cache, const float* row, int t) {
@@ -364,8 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
         return;
     }
     const float* row = p.scores + int64_t(b) * p.row_width;
-    if (n <= kRegCap && pad_slot(n) <= cache_cap)
-        select_row_regs(sm, cache, row, n, k, out);
+    if (n <= kRegCap && pad_slot(n) <= cache_cap) {
+        if (!select_row_sampled(sm, cache, cache_cap, row, n, k, out)) {
+            __syncthreads();
+            select_row_regs(sm, cache, row, n, k, out);
+        }
+    }
     else if (n <= cache_cap)
         select_row<true>(sm, cache, row, n, k, out);
     else

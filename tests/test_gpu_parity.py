@@ -160,3 +160,41 @@ def test_repeat_runs_bitwise_deterministic(gpu_lib):
     s1, t1 = _run_all(gpu_lib, case)
     np.testing.assert_array_equal(s0.view(np.uint32), s1.view(np.uint32))
     np.testing.assert_array_equal(t0, t1)
+
+
+def _topk_on_rows(b, rows, n_live, k):
+    """The top-k entry point on crafted fp32 rows (row width = rows.shape[1])."""
+    import torch
+    B, M = rows.shape
+    s = torch.from_numpy(np.ascontiguousarray(rows, dtype=np.float32)).cuda()
+    seq = torch.from_numpy((np.asarray(n_live, dtype=np.int64) * 4).astype(np.int32)).cuda()
+    t = b.dsa_indexer_topk(s, seq, 4 * M, k)
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def test_topk_rows_that_defeat_the_sample(gpu_lib, oracle):
+    """Rows where every 4th position scores high (too few keys pass the sampled threshold),
+    rows with all scores equal (too many pass), heavy ties, and ragged live lengths: every
+    path of the top-k kernel must give the exact top-k (ties to the lower position)."""
+    rng = np.random.default_rng(99)
+    M, k = 32768, 2048
+    rows, n_live = [], []
+    r = rng.standard_normal(M).astype(np.float32)
+    r[0::4] += 100.0
+    rows.append(r); n_live.append(M)                       # samples all high: fallback (too few)
+    rows.append(np.full(M, 1.5, np.float32)); n_live.append(M)   # one value: fallback (too many)
+    rows.append(np.floor(rng.standard_normal(M) * 3).astype(np.float32)); n_live.append(M)  # ties
+    r = rng.standard_normal(M).astype(np.float32)
+    rows.append(r); n_live.append(30001)                   # ragged, n % 4 == 1
+    r = rng.standard_normal(M).astype(np.float32)
+    r[:8] = 50.0
+    rows.append(r); n_live.append(2051)                    # barely more than k
+    r = -np.abs(rng.standard_normal(M)).astype(np.float32)
+    r[::7] = -0.0
+    rows.append(r); n_live.append(M)                       # negative scores and (only negative) zeros
+    rows = np.stack(rows)
+    got = _topk_on_rows(gpu_lib, rows, n_live, k)
+    for i, n in enumerate(n_live):
+        ref = oracle.topk_row(rows[i].astype(np.float64), n, k)
+        np.testing.assert_array_equal(got[i], ref, err_msg=f"row {i}")
