@@ -56,6 +56,9 @@ def parse_args(argv=None):
     ap.add_argument("--reference-rows-per-step", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context-scaling", action="store_true")
+    ap.add_argument("--l2-flush", action="store_true",
+                    help="memset a 512 MiB buffer before every timed launch (default: back-to-back steps; "
+                         "the live keys are twice the L2)")
     return ap.parse_args(argv)
 
 
@@ -239,12 +242,14 @@ def context_scaling(binding, inputs, device):
             "workload": "64 requests x 512 tokens, k=2048, same keys and page ids; CUDA-graph replay"}
 
 
-def workload_config(case, world):
+def workload_config(case, world, l2_flush=False):
     live = int(case.live_positions().sum())
     return {"workload": case.name, "batch": case.batch, "max_context": case.max_context,
             "seq_len": int(case.seq_lens.max()), "k": case.k, "pool_pages": case.num_pages,
             "live_positions": live, "live_key_bytes": live * KEY_BYTES_PER_POSITION,
-            "l2": "flushed between steps (512 MiB memset, outside the events); inputs 2x L2",
+            "l2": ("flushed before every timed launch (512 MiB memset, outside the events)" if l2_flush else
+                   "not flushed: back-to-back steps, live keys 268 MB = 2x the 129 MB L2 (DRAM bytes per "
+                   "launch = algorithmic, ncu with --cache-control none)"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
@@ -308,7 +313,7 @@ def run_ours(args):
     scores = torch.empty((B, M), dtype=torch.float32, device=device)
     topk = torch.empty((B, K), dtype=torch.int32, device=device)
     ws = binding.new_workspace(B, case.max_context, K, device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = torch.empty(FLUSH_BYTES if args.l2_flush else 1, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
     def step():
@@ -318,10 +323,14 @@ def run_ours(args):
     def scores_only():
         binding.dsa_indexer_scores(q, w, pool, table, seq, case.max_context, scores=scores, workspace=ws)
 
+    def maybe_flush():
+        if args.l2_flush:
+            flush.zero_()
+
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
+        maybe_flush()
         step()
-        flush.zero_()
+        maybe_flush()
         scores_only()
     torch.cuda.synchronize(device)
     if binding.get_error(ws) != 0:
@@ -336,7 +345,7 @@ def run_ours(args):
         clocks.mark_start()
         wall0 = time.perf_counter()
         for i in range(n):
-            flush.zero_()
+            maybe_flush()
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
@@ -355,7 +364,7 @@ def run_ours(args):
     n_k = max(10, min(n, 500))
     evk = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_k)]
     for i in range(n_k):
-        flush.zero_()
+        maybe_flush()
         evk[i][0].record(stream)
         scores_only()
         evk[i][1].record(stream)
@@ -387,7 +396,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.fmean(t_step), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(case, world),
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(case, world, args.l2_flush),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "kernel": "scores_kernel",
                      "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
