@@ -49,6 +49,16 @@
  * H, D and E are parameters (the indexer uses 32, 64, 64) so that the pins
  * can run the definition on tiny hand-checkable shapes.
  *
+ * fp8 key cache.  The deployment described in "The Indexer O(max_context)
+ * Breakthrough" (section "The Indexer O(max_context) Breakthrough", the
+ * per-op discussion of precision boundaries) keeps an fp8 KV cache; the pages
+ * give no scale format.  Reading used here: each C4 key is stored as 64
+ * OCP e4m3 codes (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent field 0 is subnormal; codes 0x7F and 0xFF are NaN) and one
+ * positive fp32 scale, and k[t, d] = scale[t] * e4m3(code[t, d]).  The score
+ * is then the same formula on these keys:
+ *   codes   uint8 [num_pages, E, D],  scales float [num_pages, E].
+ *
  * Pins: every function here is checked by the non-GPU tests against closed
  * forms, invariants, a hand-worked example and library routines.
  */
@@ -69,6 +79,22 @@ double dsa_oracle_bf16_to_double(uint16_t bits)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* OCP fp8 e4m3 code -> double (exact).  NaN codes return NaN. */
+double dsa_oracle_e4m3_to_double(uint8_t code)
+{
+    const int sign = (code >> 7) & 1;
+    const int exp = (code >> 3) & 0xF;
+    const int man = code & 0x7;
+    double v;
+    if (exp == 0xF && man == 0x7)
+        return NAN;
+    if (exp == 0)
+        v = ldexp((double)man, -9); /* subnormal: man / 8 * 2^(1 - 7) */
+    else
+        v = ldexp(1.0 + (double)man / 8.0, exp - 7);
+    return sign ? -v : v;
 }
 
 /* Step 1: C4 keys that hold data for a request of seq_len tokens. */
@@ -151,6 +177,60 @@ int dsa_oracle_scores(const uint16_t *q, const float *w, int32_t H, int32_t D,
         }
         int64_t n = dsa_oracle_live_count(seq_lens[b]);
         rc = dsa_oracle_gather(pool, num_pages, E, D, page_table + (int64_t)b * W, W, n, keys);
+        if (rc != ORACLE_OK)
+            break;
+        dsa_oracle_scores_dense(q + (int64_t)b * H * D, w + (int64_t)b * H, H, D, keys, n, M,
+                                scores + (int64_t)b * M);
+    }
+    free(keys);
+    return rc;
+}
+
+/*
+ * Step 2 for the fp8 cache: contiguous keys of one request, each the entry's
+ * scale times its decoded codes.
+ */
+int dsa_oracle_gather_fp8(const uint8_t *codes, const float *scales, int64_t num_pages, int32_t E,
+                          int32_t D, const int32_t *table_row, int64_t W, int64_t n, double *keys_out)
+{
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t j = t / E;
+        int64_t e = t % E;
+        if (j >= W)
+            return ORACLE_BAD_ARG;
+        int64_t page = table_row[j];
+        if (page < 0 || page >= num_pages)
+            return ORACLE_BAD_PAGE;
+        const uint8_t *src = codes + (page * E + e) * D;
+        double scale = (double)scales[page * E + e];
+        for (int32_t d = 0; d < D; ++d)
+            keys_out[t * D + d] = scale * dsa_oracle_e4m3_to_double(src[d]);
+    }
+    return ORACLE_OK;
+}
+
+/* Steps 1-4 for a batch on the fp8 cache: scores double [B, M]. */
+int dsa_oracle_scores_fp8(const uint16_t *q, const float *w, int32_t H, int32_t D,
+                          const uint8_t *codes, const float *scales, int64_t num_pages, int32_t E,
+                          const int32_t *page_table, const int32_t *seq_lens, int32_t B,
+                          int64_t max_context, double *scores)
+{
+    if (B < 0 || H <= 0 || D <= 0 || E <= 0 || max_context <= 0 || max_context % (4 * E) != 0)
+        return ORACLE_BAD_ARG;
+    int64_t M = max_context / 4;
+    int64_t W = max_context / (4 * E);
+    double *keys = (double *)malloc((size_t)(M > 0 ? M : 1) * (size_t)D * sizeof(double));
+    if (!keys)
+        return ORACLE_NO_MEMORY;
+    int rc = ORACLE_OK;
+    for (int32_t b = 0; b < B; ++b) {
+        if (seq_lens[b] > max_context) {
+            rc = ORACLE_BAD_ARG;
+            break;
+        }
+        int64_t n = dsa_oracle_live_count(seq_lens[b]);
+        rc = dsa_oracle_gather_fp8(codes, scales, num_pages, E, D, page_table + (int64_t)b * W, W, n,
+                                   keys);
         if (rc != ORACLE_OK)
             break;
         dsa_oracle_scores_dense(q + (int64_t)b * H * D, w + (int64_t)b * H, H, D, keys, n, M,

@@ -52,6 +52,12 @@ def _load():
         lib.dsa_oracle_topk_row.restype = ctypes.c_int
         lib.dsa_oracle_topk.argtypes = [p, p, i32, i64, i32, p]
         lib.dsa_oracle_topk.restype = ctypes.c_int
+        lib.dsa_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.dsa_oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.dsa_oracle_gather_fp8.argtypes = [p, p, i64, i32, i32, p, i64, i64, p]
+        lib.dsa_oracle_gather_fp8.restype = ctypes.c_int
+        lib.dsa_oracle_scores_fp8.argtypes = [p, p, i32, i32, p, p, i64, i32, p, p, i32, i64, p]
+        lib.dsa_oracle_scores_fp8.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -129,6 +135,45 @@ def topk(rows, seq_lens, max_context: int, k: int) -> np.ndarray:
     out = np.empty((B, k), dtype=np.int32)
     _check(_load().dsa_oracle_topk(_ptr(rows), _ptr(seq), B, max_context, k, _ptr(out)), "topk")
     return out
+
+
+def e4m3_to_double(code: int) -> float:
+    return float(_load().dsa_oracle_e4m3_to_double(int(code)))
+
+
+def gather_fp8(codes, scales, table_row, n: int, entries: int = 64) -> np.ndarray:
+    """Contiguous fp64 keys [n, D] (scale x decoded codes) of one request."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    table_row = np.ascontiguousarray(table_row, dtype=np.int32)
+    D = codes.shape[-1]
+    out = np.empty((max(n, 0), D), dtype=np.float64)
+    rc = _load().dsa_oracle_gather_fp8(_ptr(codes), _ptr(scales), codes.shape[0], entries, D,
+                                       _ptr(table_row), table_row.shape[0], n, _ptr(out))
+    _check(rc, "gather_fp8")
+    return out
+
+
+def scores_fp8(q, w, key_codes, key_scales, page_table, seq_lens, max_context: int) -> np.ndarray:
+    """fp64 scores [B, max_context/4] on the fp8 cache (k = scale x e4m3(code))."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    codes = np.ascontiguousarray(key_codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(key_scales, dtype=np.float32)
+    table = np.ascontiguousarray(page_table, dtype=np.int32)
+    seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, H, D = q.shape
+    E = codes.shape[1]
+    out = np.empty((B, max_context // 4), dtype=np.float64)
+    rc = _load().dsa_oracle_scores_fp8(_ptr(q), _ptr(w), H, D, _ptr(codes), _ptr(scales), codes.shape[0], E,
+                                       _ptr(table), _ptr(seq), B, max_context, _ptr(out))
+    _check(rc, "scores_fp8")
+    return out
+
+
+def case_scores_fp8(case) -> np.ndarray:
+    return scores_fp8(case.q, case.w, case.key_codes, case.key_scales, case.page_table, case.seq_lens,
+                      case.max_context)
 
 
 def case_scores(case) -> np.ndarray:

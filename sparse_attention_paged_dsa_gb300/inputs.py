@@ -49,6 +49,38 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def _e4m3_table() -> np.ndarray:
+    """Values of the positive finite OCP e4m3 codes 0x00..0x7E (index = code)."""
+    vals = np.empty(0x7F, dtype=np.float64)
+    for c in range(0x7F):
+        e, m = c >> 3, c & 7
+        vals[c] = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return vals
+
+
+_E4M3 = _e4m3_table()
+
+
+def f32_to_e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest OCP e4m3 value (ties to the even code), saturating at +-448; uint8 codes."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.clip(np.searchsorted(_E4M3, a, side="left"), 0, 0x7E)
+    lo = np.clip(hi - 1, 0, 0x7E)
+    d_lo = a - _E4M3[lo]
+    d_hi = _E4M3[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(x) & (code != 0), code | np.uint8(0x80), code).astype(np.uint8)
+
+
+def e4m3_codes_to_f32(c: np.ndarray) -> np.ndarray:
+    """Exact values of e4m3 codes (no NaN codes expected)."""
+    c = np.asarray(c, dtype=np.uint8)
+    v = _E4M3[c & 0x7F]
+    return np.where(c & 0x80, -v, v).astype(np.float32)
+
+
 @dataclasses.dataclass
 class IndexerCase:
     """One batch of indexer inputs, all host numpy arrays, C-contiguous.
@@ -71,6 +103,8 @@ class IndexerCase:
     max_context: int
     k: int
     seed: int = 0
+    key_codes: np.ndarray = None   # uint8 [P, 64, 64] e4m3 codes (fp8 cache), or None
+    key_scales: np.ndarray = None  # float32 [P, 64] positive per-key scales (fp8 cache), or None
 
     @property
     def batch(self) -> int:
@@ -198,6 +232,25 @@ def make_case(
         k=k,
         seed=seed,
     )
+
+
+def with_fp8_keys(case: IndexerCase, scale: str = "absmax") -> IndexerCase:
+    """The same case with an fp8 key cache made from its bf16 keys.
+
+    scale "absmax": each key's scale is max|k| / 448 (1.0 for an all-zero key), codes are
+    e4m3(k / scale); scale "one": scale 1.0 and codes e4m3(k) (exact for small integers).
+    """
+    k = bf16_bits_to_f32(case.key_pool).astype(np.float64)
+    if scale == "absmax":
+        amax = np.max(np.abs(k), axis=-1)
+        sc = np.where(amax > 0, amax / 448.0, 1.0).astype(np.float32)
+    elif scale == "one":
+        sc = np.ones(k.shape[:-1], dtype=np.float32)
+    else:
+        raise ValueError(scale)
+    codes = f32_to_e4m3_codes(k / sc.astype(np.float64)[..., None])
+    return dataclasses.replace(case, name=case.name + "_fp8", key_codes=np.ascontiguousarray(codes),
+                               key_scales=np.ascontiguousarray(sc))
 
 
 # The five workloads of the decode indexer, named by what they are.
