@@ -316,8 +316,8 @@ def test_stored_oracle_values_reproduce():
 
 # ------------------------------------------------------ planted-slip check
 MUTATIONS = [
-    ("page index uses t % E", "int64_t j = t / E;", "int64_t j = t % E;"),
-    ("entry index uses t / E", "int64_t e = t % E;", "int64_t e = t / E;"),
+    ("page index uses t % E", "int64_t j = t / E;  /* page slot", "int64_t j = t % E;  /* page slot"),
+    ("entry index uses t / E", "int64_t e = t % E;  /* entry", "int64_t e = t / E;  /* entry"),
     ("relu dropped", "double r = dot > 0.0 ? dot : 0.0;", "double r = dot;"),
     ("weight dropped", "s += (double)w_row[h] * r;", "s += r;"),
     ("floor in place of ceil", "return (seq_len + 3) / 4;", "return seq_len / 4;"),
