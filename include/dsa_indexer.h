@@ -168,6 +168,37 @@ DSA_API dsa_status_t dsa_indexer_fused_noalloc(const void *q, const float *w, co
                                        int32_t k, int32_t *topk_idx, void *stream);
 
 /*
+ * fp8 key cache.  The deployment on the pages keeps its KV cache in fp8
+ * ("The Indexer O(max_context) Breakthrough", section "The Indexer
+ * O(max_context) Breakthrough"); the pages do not give the index-key format.
+ * This library's format: each C4 key is 64 OCP e4m3 codes (bias 7, no
+ * infinities, 0x7F/0xFF NaN) and one fp32 scale, k[t, d] = scale[t] x
+ * e4m3(code[t, d]).  Layouts (C-contiguous):
+ *     key_codes   uint8 [num_pages, 64, 64]  (page, entry, dim), 16-byte aligned
+ *     key_scales  fp32  [num_pages, 64]      (page, entry),      16-byte aligned
+ * Scales of live keys must be positive and finite: the kernel computes
+ * scale[t] x sum_h w[b, h] x max(0, q[b, h, :] . e4m3(code[t, :])), which
+ * equals step 2 on k = scale x e4m3(code) exactly when scale > 0.  Codes and
+ * scales of entries past the live length, or of pages no live slot names,
+ * are never used (NaN there does not leak).  Everything else (q, w,
+ * page_table, seq_lens, outputs, workspace, error bits, capture safety) is
+ * as for the bf16 entry points above.  A key costs 68 bytes instead of 128.
+ */
+DSA_API dsa_status_t dsa_indexer_scores_fp8(const void *q, const float *w, const void *key_codes,
+                                    const float *key_scales, int64_t num_pages,
+                                    const int32_t *page_table, const int32_t *seq_lens,
+                                    int32_t batch, int64_t max_context, float *scores,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* dsa_indexer_fused on the fp8 key cache (same outputs, same workspace rule). */
+DSA_API dsa_status_t dsa_indexer_fused_fp8(const void *q, const float *w, const void *key_codes,
+                                   const float *key_scales, int64_t num_pages,
+                                   const int32_t *page_table, const int32_t *seq_lens,
+                                   int32_t batch, int64_t max_context, int32_t k,
+                                   int32_t *topk_idx, float *scores_opt, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
  * Read the sticky device error word into *code (host pointer).  Synchronises
  * `stream` (not capture-safe).  clear != 0 zeroes the word afterwards.
  */

@@ -56,6 +56,10 @@ def load():
     lib.dsa_indexer_topk.restype = st
     lib.dsa_indexer_fused.argtypes = [p, p, p, i64, p, p, i32, i64, i32, p, p, p, sz, p]
     lib.dsa_indexer_fused.restype = st
+    lib.dsa_indexer_scores_fp8.argtypes = [p, p, p, p, i64, p, p, i32, i64, p, p, sz, p]
+    lib.dsa_indexer_scores_fp8.restype = st
+    lib.dsa_indexer_fused_fp8.argtypes = [p, p, p, p, i64, p, p, i32, i64, i32, p, p, p, sz, p]
+    lib.dsa_indexer_fused_fp8.restype = st
     lib.dsa_indexer_get_error.argtypes = [p, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, p]
     lib.dsa_indexer_get_error.restype = st
     lib.dsa_status_string.argtypes = [st]
@@ -170,6 +174,59 @@ def dsa_indexer_fused(q, w, key_pool, page_table, seq_lens, max_context: int, k:
     return topk_idx
 
 
+_FP8 = tuple(t for t in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if t is not None)
+
+
+def _fp8_args(q, w, key_codes, key_scales, page_table, seq_lens, max_context):
+    B = q.shape[0]
+    _need(q, "q", _BF16, (B, HEADS, HEAD_DIM))
+    _need(w, "w", (torch.float32,), (B, HEADS))
+    _need(key_codes, "key_codes", _FP8)
+    if key_codes.dim() != 3 or tuple(key_codes.shape[1:]) != (PAGE_ENTRIES, HEAD_DIM):
+        raise ValueError(f"key_codes must be [num_pages, 64, 64], got {tuple(key_codes.shape)}")
+    _need(key_scales, "key_scales", (torch.float32,), (key_codes.shape[0], PAGE_ENTRIES))
+    _need(page_table, "page_table", (torch.int32,), (B, max_context // PAGE_TOKENS))
+    _need(seq_lens, "seq_lens", (torch.int32,), (B,))
+    return B
+
+
+def dsa_indexer_scores_fp8(q, w, key_codes, key_scales, page_table, seq_lens, max_context: int, scores=None,
+                           workspace=None):
+    """Scores on the fp8 key cache (e4m3 codes + per-key fp32 scale), as ``dsa_indexer_scores``."""
+    B = _fp8_args(q, w, key_codes, key_scales, page_table, seq_lens, max_context)
+    M = max_context // 4
+    if scores is None:
+        scores = torch.empty((B, M), dtype=torch.float32, device=q.device)
+    _need(scores, "scores", (torch.float32,), (B, M))
+    if workspace is None:
+        workspace = torch.zeros(WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=q.device)
+    st = load().dsa_indexer_scores_fp8(_ptr(q), _ptr(w), _ptr(key_codes), _ptr(key_scales), key_codes.shape[0],
+                                       _ptr(page_table), _ptr(seq_lens), B, max_context, _ptr(scores),
+                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(q.device))
+    _check(st, "dsa_indexer_scores_fp8")
+    return scores
+
+
+def dsa_indexer_fused_fp8(q, w, key_codes, key_scales, page_table, seq_lens, max_context: int, k: int,
+                          topk_idx=None, scores=None, workspace=None):
+    """Scores + top-k on the fp8 key cache, as ``dsa_indexer_fused``."""
+    B = _fp8_args(q, w, key_codes, key_scales, page_table, seq_lens, max_context)
+    if topk_idx is None:
+        topk_idx = torch.empty((B, k), dtype=torch.int32, device=q.device)
+    _need(topk_idx, "topk_idx", (torch.int32,), (B, k))
+    if scores is not None:
+        _need(scores, "scores", (torch.float32,), (B, max_context // 4))
+    if workspace is None:
+        workspace = new_workspace(B, max_context, k, q.device)
+    st = load().dsa_indexer_fused_fp8(_ptr(q), _ptr(w), _ptr(key_codes), _ptr(key_scales), key_codes.shape[0],
+                                      _ptr(page_table), _ptr(seq_lens), B, max_context, k, _ptr(topk_idx),
+                                      _ptr(scores), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(q.device))
+    _check(st, "dsa_indexer_fused_fp8")
+    return topk_idx
+
+
 def get_error(workspace, clear: bool = True) -> int:
     """Read (and by default clear) the sticky device error word; synchronises the stream."""
     code = ctypes.c_uint32(0)
@@ -187,3 +244,10 @@ def to_device(case, device="cuda"):
     table = torch.from_numpy(case.page_table).to(device)
     seq = torch.from_numpy(case.seq_lens).to(device)
     return q, w, pool, table, seq
+
+
+def to_device_fp8(case, device="cuda"):
+    """Device copies of an fp8 case's key codes (uint8) and key scales (fp32)."""
+    if case.key_codes is None or case.key_scales is None:
+        raise ValueError("case has no fp8 key cache (see inputs.with_fp8_keys)")
+    return torch.from_numpy(case.key_codes).to(device), torch.from_numpy(case.key_scales).to(device)

@@ -64,6 +64,39 @@ dsa_status_t make_keys_map(CUtensorMap* map, const void* key_pool, int64_t num_p
     return DSA_OK;
 }
 
+// fp8 key cache: codes [num_pages, 64, 64] uint8 as a 3-D tensor (dim, entry,
+// page), one box = one page of codes, unswizzled (the kernel widens them to
+// bf16 itself); scales [num_pages, 64] fp32, one box = the page's 64 scales.
+dsa_status_t make_fp8_maps(CUtensorMap* codes_map, CUtensorMap* scales_map, const void* key_codes,
+                           const float* key_scales, int64_t num_pages) {
+    auto enc = encode_tiled();
+    if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled lookup");
+    const cuuint64_t cdims[3] = {cuuint64_t(kHeadDim), cuuint64_t(kPageEntries), cuuint64_t(num_pages)};
+    const cuuint64_t cstrides[2] = {cuuint64_t(kHeadDim), cuuint64_t(kPageEntries * kHeadDim)};
+    const cuuint32_t cbox[3] = {cuuint32_t(kHeadDim), cuuint32_t(kPageEntries), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(codes_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(key_codes), cdims, cstrides,
+                     cbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled(codes): CUresult %d",
+                      int(r));
+        return DSA_ERR_CUDA;
+    }
+    const cuuint64_t sdims[2] = {cuuint64_t(kPageEntries), cuuint64_t(num_pages)};
+    const cuuint64_t sstrides[1] = {cuuint64_t(kPageEntries * sizeof(float))};
+    const cuuint32_t sbox[2] = {cuuint32_t(kPageEntries), 1};
+    r = enc(scales_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(key_scales), sdims, sstrides, sbox,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled(scales): CUresult %d",
+                      int(r));
+        return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+}
+
 // Query [batch * 32, 64] bf16; one box = the 32 heads of one request.
 dsa_status_t make_q_map(CUtensorMap* map, const void* q, int32_t batch) {
     auto enc = encode_tiled();
@@ -104,14 +137,9 @@ dsa_status_t check_score_inputs(const void* q, const float* w, const void* key_p
     return DSA_OK;
 }
 
-dsa_status_t run_scores(const void* q, const float* w, const void* key_pool, int64_t num_pages,
-                        const int32_t* page_table, const int32_t* seq_lens, int32_t batch, int64_t max_context,
-                        float* out, int fill_dead, void* workspace, cudaStream_t stream) {
-    CUtensorMap keys_map, q_map;
-    dsa_status_t st = make_keys_map(&keys_map, key_pool, num_pages);
-    if (st != DSA_OK) return st;
-    st = make_q_map(&q_map, q, batch);
-    if (st != DSA_OK) return st;
+dsa::ScoresParams score_params(const float* w, int64_t num_pages, const int32_t* page_table,
+                               const int32_t* seq_lens, int32_t batch, int64_t max_context, float* out,
+                               int fill_dead, void* workspace) {
     dsa::ScoresParams p{};
     p.page_table = page_table;
     p.seq_lens = seq_lens;
@@ -124,8 +152,35 @@ dsa_status_t run_scores(const void* q, const float* w, const void* key_pool, int
     p.table_width = int32_t(max_context / DSA_PAGE_TOKENS);
     p.batch = batch;
     p.fill_dead = fill_dead;
+    return p;
+}
+
+dsa_status_t run_scores(const void* q, const float* w, const void* key_pool, int64_t num_pages,
+                        const int32_t* page_table, const int32_t* seq_lens, int32_t batch, int64_t max_context,
+                        float* out, int fill_dead, void* workspace, cudaStream_t stream) {
+    CUtensorMap keys_map, q_map;
+    dsa_status_t st = make_keys_map(&keys_map, key_pool, num_pages);
+    if (st != DSA_OK) return st;
+    st = make_q_map(&q_map, q, batch);
+    if (st != DSA_OK) return st;
+    const dsa::ScoresParams p =
+        score_params(w, num_pages, page_table, seq_lens, batch, max_context, out, fill_dead, workspace);
     const cudaError_t e = dsa::launch_scores(keys_map, q_map, p, stream);
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "scores kernel launch");
+}
+
+dsa_status_t run_scores_fp8(const void* q, const float* w, const void* key_codes, const float* key_scales,
+                            int64_t num_pages, const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                            int64_t max_context, float* out, int fill_dead, void* workspace, cudaStream_t stream) {
+    CUtensorMap codes_map, scales_map, q_map;
+    dsa_status_t st = make_fp8_maps(&codes_map, &scales_map, key_codes, key_scales, num_pages);
+    if (st != DSA_OK) return st;
+    st = make_q_map(&q_map, q, batch);
+    if (st != DSA_OK) return st;
+    const dsa::ScoresParams p =
+        score_params(w, num_pages, page_table, seq_lens, batch, max_context, out, fill_dead, workspace);
+    const cudaError_t e = dsa::launch_scores_fp8(codes_map, scales_map, q_map, p, stream);
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "fp8 scores kernel launch");
 }
 
 dsa_status_t run_topk(const float* scores, const int32_t* seq_lens, int32_t batch, int64_t max_context, int32_t k,
@@ -207,6 +262,46 @@ dsa_status_t dsa_indexer_fused(const void* q, const float* w, const void* key_po
                              : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kWorkspaceHeaderBytes);
     st = run_scores(q, w, key_pool, num_pages, page_table, seq_lens, batch, max_context, rows, scores_opt ? 1 : 0,
                     workspace, s);
+    if (st != DSA_OK) return st;
+    return run_topk(rows, seq_lens, batch, max_context, k, topk_idx, workspace, s);
+}
+
+dsa_status_t dsa_indexer_scores_fp8(const void* q, const float* w, const void* key_codes, const float* key_scales,
+                                    int64_t num_pages, const int32_t* page_table, const int32_t* seq_lens,
+                                    int32_t batch, int64_t max_context, float* scores, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    dsa_status_t st = check_shape(batch, max_context);
+    if (st != DSA_OK) return st;
+    st = check_score_inputs(q, w, key_codes, num_pages, page_table, seq_lens);
+    if (st != DSA_OK) return st;
+    if (!key_scales || !aligned(key_scales, 16)) return DSA_ERR_INVALID_ARG;
+    if (!scores || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
+    st = check_workspace(workspace, workspace_bytes, dsa::kWorkspaceHeaderBytes);
+    if (st != DSA_OK) return st;
+    return run_scores_fp8(q, w, key_codes, key_scales, num_pages, page_table, seq_lens, batch, max_context, scores, 1,
+                          workspace, static_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_indexer_fused_fp8(const void* q, const float* w, const void* key_codes, const float* key_scales,
+                                   int64_t num_pages, const int32_t* page_table, const int32_t* seq_lens,
+                                   int32_t batch, int64_t max_context, int32_t k, int32_t* topk_idx,
+                                   float* scores_opt, void* workspace, size_t workspace_bytes, void* stream) {
+    dsa_status_t st = check_shape(batch, max_context);
+    if (st != DSA_OK) return st;
+    st = check_score_inputs(q, w, key_codes, num_pages, page_table, seq_lens);
+    if (st != DSA_OK) return st;
+    if (!key_scales || !aligned(key_scales, 16)) return DSA_ERR_INVALID_ARG;
+    if (!topk_idx || !aligned(topk_idx, 4)) return DSA_ERR_INVALID_ARG;
+    if (scores_opt && !aligned(scores_opt, 16)) return DSA_ERR_INVALID_ARG;
+    if (k < 1 || int64_t(k) > max_context / 4) return DSA_ERR_INVALID_ARG;
+    const size_t need = scores_opt ? dsa::kWorkspaceHeaderBytes : dsa_indexer_workspace_size(batch, max_context, k);
+    st = check_workspace(workspace, workspace_bytes, need);
+    if (st != DSA_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* rows = scores_opt ? scores_opt
+                             : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kWorkspaceHeaderBytes);
+    st = run_scores_fp8(q, w, key_codes, key_scales, num_pages, page_table, seq_lens, batch, max_context, rows,
+                        scores_opt ? 1 : 0, workspace, s);
     if (st != DSA_OK) return st;
     return run_topk(rows, seq_lens, batch, max_context, k, topk_idx, workspace, s);
 }

@@ -13,6 +13,8 @@ constexpr int kHeads = 32;
 constexpr int kHeadDim = 64;
 constexpr int kPageEntries = 64;                          // C4 keys per page
 constexpr int kPageBytes = kPageEntries * kHeadDim * 2;   // 8 KiB of bf16
+constexpr int kPageCodeBytes = kPageEntries * kHeadDim;   // 4 KiB of e4m3 codes (fp8 cache)
+constexpr int kPageScaleBytes = kPageEntries * 4;         // 256 B of fp32 key scales (fp8 cache)
 constexpr int kQRowBytes = kHeads * kHeadDim * 2;         // 4 KiB of bf16
 constexpr int kUnitPositions = 2 * kPageEntries;          // one work unit = 2 pages = 128 keys
 constexpr int kMaxBatch = 1024;
@@ -51,6 +53,11 @@ struct TopkParams {
 // Scores kernel: persistent, one CTA per SM, TMA page gather + tcgen05 QK.
 cudaError_t launch_scores(const CUtensorMap& keys_map, const CUtensorMap& q_map, const ScoresParams& p,
                           cudaStream_t stream);
+
+// Scores kernel on the fp8 key cache (e4m3 codes + per-key fp32 scale): the
+// codes are widened to bf16 in shared memory before the same tcgen05 QK.
+cudaError_t launch_scores_fp8(const CUtensorMap& codes_map, const CUtensorMap& scales_map, const CUtensorMap& q_map,
+                              const ScoresParams& p, cudaStream_t stream);
 
 // Top-k kernel: one CTA per request row, radix select over live positions.
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);

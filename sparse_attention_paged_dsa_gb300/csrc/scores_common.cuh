@@ -1,0 +1,180 @@
+// scores_common.cuh -- pieces shared by the bf16 and fp8 scores kernels:
+// per-request live extents, the work-unit schedule, page-id preparation,
+// unit metadata, the dead-tail -inf fill and the schedule reset.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "indexer_kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace dsa {
+namespace scores {
+
+constexpr int kBatch = 32;         // units prepared per warp-wide page-table load
+constexpr int kChunk = 2;          // units per dynamic scheduling step
+constexpr int kStaticEighths = 7;  // share of the units assigned statically
+constexpr int kEndOfWork = -1;     // metadata marker: no more units
+static_assert(kChunk >= 1 && kChunk <= kBatch, "a chunk is prepared by one warp");
+
+// Scheduling words in the 256-byte workspace header (word 0 is the error word).
+constexpr int kHeaderNextChunkWord = 32;  // byte 128
+constexpr int kHeaderExitWord = 48;       // byte 192
+
+// Unit metadata: request (10 bits), page pair within the request (15 bits),
+// validity of its two pages (2 bits).  Max row width 2^22 C4 positions keeps
+// the pair below 2^15; kMaxBatch = 1024 keeps the request below 2^10.
+__device__ __forceinline__ int pack_meta(int b, int pair, bool ok0, bool ok1) {
+    return (b << 17) | (pair << 2) | (ok1 ? 2 : 0) | (ok0 ? 1 : 0);
+}
+__device__ __forceinline__ int meta_row(int m) { return m >> 17; }
+__device__ __forceinline__ int meta_pair(int m) { return (m >> 2) & 0x7FFF; }
+
+// Live C4 count and first work unit of every request (in shared memory).
+struct RowTable {
+    int32_t n_live[kMaxBatch];
+    int32_t unit_start[kMaxBatch + 1];
+};
+
+// One warp fills the table: n_b = ceil(clamp(seq_len_b, 0, max_context) / 4), units of
+// kUnitPositions positions, exclusive prefix of units.  Flags clamped lengths (CTA 0).
+__device__ __forceinline__ void build_row_table(RowTable& t, const ScoresParams& p, int lane) {
+    const int batch = p.batch;
+    const int per = (batch + 31) / 32;  // lane l owns rows [l*per, (l+1)*per)
+    const int b0 = min(lane * per, batch), b1 = min(b0 + per, batch);
+    int units = 0;
+    bool clamped = false;
+    for (int b = b0; b < b1; ++b) {
+        int64_t s = p.seq_lens[b];
+        if (s < 0 || s > p.max_context) clamped = true;
+        s = s < 0 ? 0 : (s > p.max_context ? p.max_context : s);
+        const int n = static_cast<int>((s + 3) >> 2);
+        t.n_live[b] = n;
+        units += (n + kUnitPositions - 1) / kUnitPositions;
+    }
+    int incl = units;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int run = incl - units;
+    for (int b = b0; b < b1; ++b) {
+        t.unit_start[b] = run;
+        run += (t.n_live[b] + kUnitPositions - 1) / kUnitPositions;
+    }
+    if (lane == 31) t.unit_start[batch] = incl;
+    if (clamped && blockIdx.x == 0) atomicOr(p.err, kErrSeqLenClamped);
+}
+
+// Largest b in [0, batch) with unit_start[b] <= u (rows without units share
+// their start with the next row, so this lands on the row that owns u).
+__device__ __forceinline__ int row_of_unit(const int32_t* unit_start, int batch, int u) {
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (unit_start[mid] <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// Bounded wait used only while draining after an abort.
+__device__ __forceinline__ void wait_landed(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
+    }
+}
+
+// One lane's unit of a batch: its request, page pair and page ids (-2: no live second page).
+struct UnitPrep {
+    int b = 0;
+    int pair = 0;
+    int pg0 = -1;
+    int pg1 = -2;
+};
+
+// Lane l prepares unit u0 + l when l < cnt (page-table loads in flight on return).
+__device__ __forceinline__ UnitPrep prepare_units(const RowTable& t, const ScoresParams& p, int u0, int cnt,
+                                                  int lane) {
+    UnitPrep c;
+    if (lane < cnt) {
+        const int u = u0 + lane;
+        c.b = row_of_unit(t.unit_start, p.batch, u);
+        c.pair = u - t.unit_start[c.b];
+        const int live_pages = (t.n_live[c.b] + kPageEntries - 1) / kPageEntries;
+        const int32_t* row = p.page_table + int64_t(c.b) * p.table_width;
+        c.pg0 = __ldg(row + 2 * c.pair);
+        c.pg1 = (2 * c.pair + 1 < live_pages) ? __ldg(row + 2 * c.pair + 1) : -2;
+    }
+    return c;
+}
+
+// The producer warp's unit schedule: first the CTA's equal contiguous share of
+// 7/8 of the units (in batches of kBatch), then kChunk-unit chunks of the last
+// eighth taken from a counter in the workspace header, each chunk number
+// requested one batch ahead.  All calls are warp-collective.
+struct UnitSchedule {
+    int sp, se, dyn0, total, ticket;
+    uint32_t* counter;
+
+    __device__ __forceinline__ UnitSchedule(const ScoresParams& p, int total_units, int lane) {
+        const int grid = gridDim.x;
+        const int S = static_cast<int>((int64_t(total_units) * kStaticEighths) / (8 * int64_t(grid)));
+        sp = blockIdx.x * S;
+        se = sp + S;
+        dyn0 = grid * S;
+        total = total_units;
+        counter = p.err + kHeaderNextChunkWord;
+        ticket = 0;
+        if (lane == 0) ticket = int(atomicAdd(counter, 1u));
+    }
+
+    // Next batch [u0, u0 + cnt); cnt == 0 when the CTA has no more work.
+    __device__ __forceinline__ void next(int& u0, int& cnt, int lane) {
+        if (sp < se) {
+            u0 = sp;
+            cnt = min(kBatch, se - sp);
+            sp += cnt;
+            return;
+        }
+        const int t = __shfl_sync(0xffffffffu, ticket, 0);
+        u0 = dyn0 + t * kChunk;
+        cnt = u0 < total ? min(kChunk, total - u0) : 0;
+        if (lane == 0 && cnt > 0) ticket = int(atomicAdd(counter, 1u));
+    }
+};
+
+// Stream -inf over every row's positions past its live units, rows split over
+// all CTAs (threads et in [0, nthreads) of each CTA take part).
+__device__ __forceinline__ void fill_dead_tails(const RowTable& t, const ScoresParams& p, int et, int nthreads) {
+    const int64_t M = p.row_width;
+    const float neg_inf = __int_as_float(0xff800000);
+    const float4 ninf4 = make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
+    const int64_t stride = int64_t(gridDim.x) * nthreads;
+    for (int b = 0; b < p.batch; ++b) {
+        const int64_t units = t.unit_start[b + 1] - t.unit_start[b];
+        const int64_t extent = units * kUnitPositions < M ? units * kUnitPositions : M;
+        float4* row = reinterpret_cast<float4*>(p.out + int64_t(b) * M);
+        for (int64_t i = extent / 4 + int64_t(blockIdx.x) * nthreads + et; i < M / 4; i += stride)
+            __stcs(row + i, ninf4);
+    }
+}
+
+// Called by one thread per CTA after all its work: the last CTA out resets
+// the schedule words for the next launch (no CTA waits for another).
+__device__ __forceinline__ void release_schedule(const ScoresParams& p) {
+    __threadfence();
+    if (atomicAdd(p.err + kHeaderExitWord, 1u) == uint32_t(gridDim.x - 1)) {
+        atomicExch(p.err + kHeaderNextChunkWord, 0u);
+        atomicExch(p.err + kHeaderExitWord, 0u);
+    }
+}
+
+}  // namespace scores
+}  // namespace dsa

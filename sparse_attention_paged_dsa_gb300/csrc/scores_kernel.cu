@@ -48,18 +48,18 @@
 #include <cstdint>
 
 #include "indexer_kernels.h"
+#include "scores_common.cuh"
 #include "sm103_ptx.cuh"
 
 
 namespace dsa {
 namespace {
 
+using namespace scores;
+
 constexpr int kStages = 4;                             // 16 KiB stages per CTA
 constexpr int kEpiGroups = 2;                          // epilogue groups of 4 warps
 constexpr int kCtasPerSm = 2;                          // two independent pipelines per SM
-constexpr int kChunk = 2;                              // units per dynamic scheduling step
-constexpr int kStaticEighths = 7;                      // share of the units assigned statically
-constexpr int kBatch = 32;                             // units prepared per warp-wide page-table load
 constexpr int kQSlots = 4;
 constexpr int kAccStages = 4;
 constexpr int kMetaRing = 16;                          // >= kStages + kAccStages + 1
@@ -69,23 +69,8 @@ constexpr int kEpiThreads = 128 * kEpiGroups;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kStageBytes = 2 * kPageBytes;            // 16 KiB: 128 keys x 128 B
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kAccCols);
-constexpr int kEndOfWork = -1;                         // metadata marker: no more units
 static_assert(kAccStages % kEpiGroups == 0, "each epilogue group owns whole accumulator stages");
 static_assert(kMetaRing >= kStages + kAccStages + 1, "metadata ring too small");
-static_assert(kChunk >= 1 && kChunk <= kBatch, "a chunk is prepared by one warp");
-
-// Unit metadata: request (10 bits), page pair within the request (15 bits),
-// validity of its two pages (2 bits).  Max row width 2^22 C4 positions keeps
-// the pair below 2^15; kMaxBatch = 1024 keeps the request below 2^10.
-__device__ __forceinline__ int pack_meta(int b, int pair, bool ok0, bool ok1) {
-    return (b << 17) | (pair << 2) | (ok1 ? 2 : 0) | (ok0 ? 1 : 0);
-}
-__device__ __forceinline__ int meta_row(int m) { return m >> 17; }
-__device__ __forceinline__ int meta_pair(int m) { return (m >> 2) & 0x7FFF; }
-
-// Scheduling words in the 256-byte workspace header (word 0 is the error word).
-constexpr int kHeaderNextChunkWord = 32;  // byte 128
-constexpr int kHeaderExitWord = 48;       // byte 192
 
 struct __align__(8) SmemCtl {
     uint64_t full[kStages];
@@ -99,59 +84,13 @@ struct __align__(8) SmemCtl {
     uint32_t tmem_base;
     int abort;
     int32_t meta[kMetaRing];
-    int32_t n_live[kMaxBatch];
-    int32_t unit_start[kMaxBatch + 1];
+    RowTable rows;
 };
 
 constexpr size_t kTileBytes = size_t(kStages) * kStageBytes + size_t(kQSlots) * kQRowBytes;
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes + sizeof(SmemCtl);
 static_assert(kSmemBytes * kCtasPerSm <= 228 * 1024, "shared memory budget per SM");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget per CTA");
-
-// Largest b in [0, batch) with unit_start[b] <= u (rows without units share
-// their start with the next row, so this lands on the row that owns u).
-__device__ __forceinline__ int row_of_unit(const int32_t* unit_start, int batch, int u) {
-    int lo = 0, hi = batch - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (unit_start[mid] <= u)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    return lo;
-}
-
-__device__ __forceinline__ void wait_landed(uint64_t* bar, uint32_t parity) {
-    const uint32_t a = smem_u32(bar);
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(a, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
-    }
-}
-
-// One lane's unit of a batch: its request, page pair and page ids (-2: no live second page).
-struct UnitPrep {
-    int b = 0;
-    int pair = 0;
-    int pg0 = -1;
-    int pg1 = -2;
-};
-
-// Lane l prepares unit u0 + l when l < cnt (page-table loads in flight on return).
-__device__ __forceinline__ UnitPrep prepare_units(const SmemCtl& ctl, const ScoresParams& p, int u0, int cnt,
-                                                  int lane) {
-    UnitPrep c;
-    if (lane < cnt) {
-        const int u = u0 + lane;
-        c.b = row_of_unit(ctl.unit_start, p.batch, u);
-        c.pair = u - ctl.unit_start[c.b];
-        const int live_pages = (ctl.n_live[c.b] + kPageEntries - 1) / kPageEntries;
-        const int32_t* row = p.page_table + int64_t(c.b) * p.table_width;
-        c.pg0 = __ldg(row + 2 * c.pair);
-        c.pg1 = (2 * c.pair + 1 < live_pages) ? __ldg(row + 2 * c.pair + 1) : -2;
-    }
-    return c;
-}
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     scores_kernel(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CUtensorMap q_map,
@@ -164,7 +103,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int batch = p.batch;
-    const int grid = gridDim.x;
 
     // ---- set-up that touches no global memory (overlaps the previous kernel).
     if (threadIdx.x == 0) {
@@ -195,41 +133,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     pdl_allow_next_grid();
 
     // ---- per-row live counts and unit prefix.
-    if (warp == 2) {
-        const int per = (batch + 31) / 32;  // lane l owns rows [l*per, (l+1)*per)
-        const int b0 = min(lane * per, batch), b1 = min(b0 + per, batch);
-        int units = 0;
-        bool clamped = false;
-        for (int b = b0; b < b1; ++b) {
-            int64_t s = p.seq_lens[b];
-            if (s < 0 || s > p.max_context) clamped = true;
-            s = s < 0 ? 0 : (s > p.max_context ? p.max_context : s);
-            const int n = static_cast<int>((s + 3) >> 2);
-            ctl.n_live[b] = n;
-            units += (n + kUnitPositions - 1) / kUnitPositions;
-        }
-        int incl = units;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int run = incl - units;
-        for (int b = b0; b < b1; ++b) {
-            ctl.unit_start[b] = run;
-            run += (ctl.n_live[b] + kUnitPositions - 1) / kUnitPositions;
-        }
-        if (lane == 31) ctl.unit_start[batch] = incl;
-        if (clamped && blockIdx.x == 0) atomicOr(p.err, kErrSeqLenClamped);
-    }
+    if (warp == 2) build_row_table(ctl.rows, p, lane);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
 
-    const int total_units = ctl.unit_start[batch];
+    const int total_units = ctl.rows.unit_start[batch];
     const uint32_t tmem_base = ctl.tmem_base;
     const int64_t M = p.row_width;
-    uint32_t* next_chunk_word = p.err + kHeaderNextChunkWord;
 
     if (warp == 0) {
         // ================= producer: schedule, page ids, TMA gathers =================
@@ -240,33 +151,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         int issued = 0, q_issued = 0, q_row = -1, seq = 0;
         bool stop = false;
 
-        // Static share: [blockIdx.x * S, (blockIdx.x + 1) * S); dynamic share: [grid * S, total) in chunks.
-        const int S = static_cast<int>((int64_t(total_units) * kStaticEighths) / (8 * int64_t(grid)));
-        int sp = blockIdx.x * S;
-        const int se = sp + S;
-        const int dyn0 = grid * S;
-        int ticket = 0;  // dynamic chunk number requested one batch ahead (lane 0)
-        if (lane == 0) ticket = int(atomicAdd(next_chunk_word, 1u));
-        auto next_batch = [&](int& u0, int& cnt) {
-            if (sp < se) {
-                u0 = sp;
-                cnt = min(kBatch, se - sp);
-                sp += cnt;
-                return;
-            }
-            const int t = __shfl_sync(0xffffffffu, ticket, 0);
-            u0 = dyn0 + t * kChunk;
-            cnt = u0 < total_units ? min(kChunk, total_units - u0) : 0;
-            if (lane == 0 && cnt > 0) ticket = int(atomicAdd(next_chunk_word, 1u));
-        };
-
+        UnitSchedule sched(p, total_units, lane);
         int cur_u0, cur_cnt;
-        next_batch(cur_u0, cur_cnt);
-        UnitPrep cur = prepare_units(ctl, p, cur_u0, cur_cnt, lane);
+        sched.next(cur_u0, cur_cnt, lane);
+        UnitPrep cur = prepare_units(ctl.rows, p, cur_u0, cur_cnt, lane);
         while (cur_cnt > 0 && !stop) {
             int nxt_u0, nxt_cnt;
-            next_batch(nxt_u0, nxt_cnt);
-            const UnitPrep nxt = prepare_units(ctl, p, nxt_u0, nxt_cnt, lane);  // loads in flight
+            sched.next(nxt_u0, nxt_cnt, lane);
+            const UnitPrep nxt = prepare_units(ctl.rows, p, nxt_u0, nxt_cnt, lane);  // loads in flight
             for (int i = 0; i < cur_cnt; ++i) {
                 const int bi = __shfl_sync(0xffffffffu, cur.b, i);
                 const int pi = __shfl_sync(0xffffffffu, cur.pair, i);
@@ -421,17 +313,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int quad = warp & 3;          // TMEM lanes [32*quad, 32*quad + 32)
         const float neg_inf = __int_as_float(0xff800000);
 
-        if (p.fill_dead) {
-            const float4 ninf4 = make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
-            const int64_t stride = int64_t(grid) * kEpiThreads;
-            for (int b = 0; b < batch; ++b) {
-                const int64_t units = ctl.unit_start[b + 1] - ctl.unit_start[b];
-                const int64_t extent = units * kUnitPositions < M ? units * kUnitPositions : M;
-                float4* row = reinterpret_cast<float4*>(p.out + int64_t(b) * M);
-                for (int64_t i = extent / 4 + int64_t(blockIdx.x) * kEpiThreads + et; i < M / 4; i += stride)
-                    __stcs(row + i, ninf4);
-            }
-        }
+        if (p.fill_dead) fill_dead_tails(ctl.rows, p, et, kEpiThreads);
 
         int cur_b = -1, n = 0;
         float wv[kHeads];
@@ -460,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     wv[4 * h4 + 2] = v.z;
                     wv[4 * h4 + 3] = v.w;
                 }
-                n = ctl.n_live[b];
+                n = ctl.rows.n_live[b];
                 cur_b = b;
             }
             const bool okf = mbar_wait(&ctl.tfull[acc], acc_phase, &ctl.abort);
@@ -495,14 +377,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     tc_fence_before_sync();
     __syncthreads();
-    if (threadIdx.x == 0) {
-        // The last CTA out resets the chunk counter for the next launch.
-        __threadfence();
-        if (atomicAdd(p.err + kHeaderExitWord, 1u) == uint32_t(grid - 1)) {
-            atomicExch(next_chunk_word, 0u);
-            atomicExch(p.err + kHeaderExitWord, 0u);
-        }
-    }
+    if (threadIdx.x == 0) release_schedule(p);
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, kTmemCols);

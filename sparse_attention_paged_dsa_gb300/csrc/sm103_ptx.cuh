@@ -68,6 +68,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// Make this thread's ordinary shared-memory stores visible to the async proxy
+// (TMA, tcgen05.mma) before it signals that the data is ready.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch
 // Block until the grid this launch depends on has completed and its memory
 // is visible (a no-op when launched without the programmatic attribute).
