@@ -37,6 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "C4 positions scored+top-k per sec and HBM GB/s (% of roofline), B=64 @128K"
 UNIT = "positions/s"
 KEY_BYTES_PER_POSITION = 128          # 64 bf16 dims of one C4 index key
+FP8_KEY_BYTES_PER_POSITION = 68       # 64 e4m3 codes + one fp32 scale (fp8 key cache)
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 512 << 20               # > 2x the 129 MB L2
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "scores_kernel_b64_ctx128k_dense.md")
@@ -56,6 +57,7 @@ def parse_args(argv=None):
     ap.add_argument("--reference-rows-per-step", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context-scaling", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the fp8 key-cache measurement")
     ap.add_argument("--l2-flush", action="store_true",
                     help="memset a 512 MiB buffer before every timed launch (default: back-to-back steps; "
                          "the live keys are twice the L2)")
@@ -242,6 +244,53 @@ def context_scaling(binding, inputs, device):
             "workload": "64 requests x 512 tokens, k=2048, same keys and page ids; CUDA-graph replay"}
 
 
+def run_fp8(args, case, binding, inputs, device, stream, live):
+    """The same workload on the fp8 key cache: fused step (events, back-to-back) and scores kernel alone."""
+    import torch
+    f = inputs.with_fp8_keys(case)
+    q, w, _, table, seq = binding.to_device(f, device)
+    codes, scales = binding.to_device_fp8(f, device)
+    B, M, K = f.batch, f.max_context // 4, f.k
+    scores = torch.empty((B, M), dtype=torch.float32, device=device)
+    topk = torch.empty((B, K), dtype=torch.int32, device=device)
+    ws = binding.new_workspace(B, f.max_context, K, device)
+
+    def step():
+        binding.dsa_indexer_fused_fp8(q, w, codes, scales, table, seq, f.max_context, K, topk_idx=topk,
+                                      scores=scores, workspace=ws)
+
+    def scores_only():
+        binding.dsa_indexer_scores_fp8(q, w, codes, scales, table, seq, f.max_context, scores=scores, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+        scores_only()
+    torch.cuda.synchronize(device)
+    n = max(10, min(args.steps, 500))
+    out = {}
+    for name, fn in (("step", step), ("scores", scores_only)):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(device)
+        out[name] = [e[0].elapsed_time(e[1]) * 1e-3 for e in ev]
+    if binding.get_error(ws) != 0:
+        raise RuntimeError("device error word set in the fp8 run")
+    peak, peak_kind = measured_hbm_peak()
+    t_step, t_scores = statistics.fmean(out["step"]), statistics.fmean(out["scores"])
+    achieved = live * FP8_KEY_BYTES_PER_POSITION / t_scores / 1e9
+    return {"value": live / t_step, "unit": UNIT, "steps": n, "ms_per_step": 1e3 * t_step,
+            "scores_kernel_us": 1e6 * t_scores,
+            "graph_us": {"scores": graph_us_per_call(scores_only), "fused": graph_us_per_call(step)},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "kernel": "scores_fp8_kernel", "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
+                         "algorithmic_bytes_per_launch": live * FP8_KEY_BYTES_PER_POSITION},
+            "cache": "e4m3 codes [pages, 64, 64] + fp32 scale per key (max|k| / 448), made from the bf16 keys",
+            "step": "dsa_indexer_fused_fp8 with the full-width scores row"}
+
+
 def workload_config(case, world, l2_flush=False):
     live = int(case.live_positions().sum())
     return {"workload": case.name, "batch": case.batch, "max_context": case.max_context,
@@ -379,6 +428,7 @@ def run_ours(args):
         e2e = run_e2e(args, case, binding, scores, topk, ws, device, stream, world, live)
 
     scaling_1m = context_scaling(binding, inputs, device) if not args.no_context_scaling else None
+    fp8 = run_fp8(args, case, binding, inputs, device, stream, live) if not args.no_fp8 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -409,6 +459,7 @@ def run_ours(args):
         "step_gbs_live_keys": live * KEY_BYTES_PER_POSITION / statistics.fmean(t_step) / 1e9,
         "cpu_baseline": cpu,
         "context_scaling": scaling_1m,
+        "fp8_key_cache": fp8,
         "e2e": e2e,
         "gpu_launches": 2 * n * world,
         "step": "dsa_indexer_fused with the full-width scores row (scores kernel, then top-k kernel)",

@@ -65,10 +65,9 @@ dsa_status_t make_keys_map(CUtensorMap* map, const void* key_pool, int64_t num_p
 }
 
 // fp8 key cache: codes [num_pages, 64, 64] uint8 as a 3-D tensor (dim, entry,
-// page), one box = one page of codes, unswizzled (the kernel widens them to
-// bf16 itself); scales [num_pages, 64] fp32, one box = the page's 64 scales.
-dsa_status_t make_fp8_maps(CUtensorMap* codes_map, CUtensorMap* scales_map, const void* key_codes,
-                           const float* key_scales, int64_t num_pages) {
+// page), one box = one page of codes stored with the 64-byte swizzle the
+// 8-bit MMA reads.  (The scales are copied by the kernel with cp.async.)
+dsa_status_t make_codes_map(CUtensorMap* codes_map, const void* key_codes, int64_t num_pages) {
     auto enc = encode_tiled();
     if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled lookup");
     const cuuint64_t cdims[3] = {cuuint64_t(kHeadDim), cuuint64_t(kPageEntries), cuuint64_t(num_pages)};
@@ -76,21 +75,10 @@ dsa_status_t make_fp8_maps(CUtensorMap* codes_map, CUtensorMap* scales_map, cons
     const cuuint32_t cbox[3] = {cuuint32_t(kHeadDim), cuuint32_t(kPageEntries), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(codes_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(key_codes), cdims, cstrides,
-                     cbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     cbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled(codes): CUresult %d",
-                      int(r));
-        return DSA_ERR_CUDA;
-    }
-    const cuuint64_t sdims[2] = {cuuint64_t(kPageEntries), cuuint64_t(num_pages)};
-    const cuuint64_t sstrides[1] = {cuuint64_t(kPageEntries * sizeof(float))};
-    const cuuint32_t sbox[2] = {cuuint32_t(kPageEntries), 1};
-    r = enc(scales_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(key_scales), sdims, sstrides, sbox,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled(scales): CUresult %d",
                       int(r));
         return DSA_ERR_CUDA;
     }
@@ -111,6 +99,38 @@ dsa_status_t make_q_map(CUtensorMap* map, const void* q, int32_t batch) {
     if (r != CUDA_SUCCESS) {
         std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled(q): CUresult %d",
                       int(r));
+        return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+}
+
+// Plain (unswizzled) maps for the fp8 kernel's query splitter: q [batch * 32,
+// 64] bf16 with one request's 32 heads per box, and w [batch, 32] fp32 with
+// one request's weights per box.
+dsa_status_t make_plain_q_w_maps(CUtensorMap* q_map, CUtensorMap* w_map, const void* q, const float* w,
+                                 int32_t batch) {
+    auto enc = encode_tiled();
+    if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled lookup");
+    const cuuint64_t qdims[2] = {cuuint64_t(kHeadDim), cuuint64_t(batch) * kHeads};
+    const cuuint64_t qstrides[1] = {cuuint64_t(kHeadDim * 2)};
+    const cuuint32_t qbox[2] = {cuuint32_t(kHeadDim), cuuint32_t(kHeads)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), qdims, qstrides, qbox, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled(q plain): CUresult %d",
+                      int(r));
+        return DSA_ERR_CUDA;
+    }
+    const cuuint64_t wdims[2] = {cuuint64_t(kHeads), cuuint64_t(batch)};
+    const cuuint64_t wstrides[1] = {cuuint64_t(kHeads * sizeof(float))};
+    const cuuint32_t wbox[2] = {cuuint32_t(kHeads), 1};
+    r = enc(w_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(w), wdims, wstrides, wbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled(w): CUresult %d", int(r));
         return DSA_ERR_CUDA;
     }
     return DSA_OK;
@@ -172,14 +192,15 @@ dsa_status_t run_scores(const void* q, const float* w, const void* key_pool, int
 dsa_status_t run_scores_fp8(const void* q, const float* w, const void* key_codes, const float* key_scales,
                             int64_t num_pages, const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
                             int64_t max_context, float* out, int fill_dead, void* workspace, cudaStream_t stream) {
-    CUtensorMap codes_map, scales_map, q_map;
-    dsa_status_t st = make_fp8_maps(&codes_map, &scales_map, key_codes, key_scales, num_pages);
+    CUtensorMap codes_map, q_map, w_map;
+    dsa_status_t st = make_codes_map(&codes_map, key_codes, num_pages);
     if (st != DSA_OK) return st;
-    st = make_q_map(&q_map, q, batch);
+    st = make_plain_q_w_maps(&q_map, &w_map, q, w, batch);
     if (st != DSA_OK) return st;
-    const dsa::ScoresParams p =
+    dsa::ScoresParams p =
         score_params(w, num_pages, page_table, seq_lens, batch, max_context, out, fill_dead, workspace);
-    const cudaError_t e = dsa::launch_scores_fp8(codes_map, scales_map, q_map, p, stream);
+    p.key_scales = key_scales;
+    const cudaError_t e = dsa::launch_scores_fp8(codes_map, q_map, w_map, p, stream);
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "fp8 scores kernel launch");
 }
 

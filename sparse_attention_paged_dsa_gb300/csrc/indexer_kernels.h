@@ -37,6 +37,7 @@ struct ScoresParams {
     int32_t table_width;        // max_context / 256
     int32_t batch;
     int32_t fill_dead;          // 1: write -inf from the live extent to the row end
+    const float* key_scales;    // [num_pages, 64] per-key scales of the fp8 cache (fp8 kernel only)
 };
 
 struct TopkParams {
@@ -54,9 +55,11 @@ struct TopkParams {
 cudaError_t launch_scores(const CUtensorMap& keys_map, const CUtensorMap& q_map, const ScoresParams& p,
                           cudaStream_t stream);
 
-// Scores kernel on the fp8 key cache (e4m3 codes + per-key fp32 scale): the
-// codes are widened to bf16 in shared memory before the same tcgen05 QK.
-cudaError_t launch_scores_fp8(const CUtensorMap& codes_map, const CUtensorMap& scales_map, const CUtensorMap& q_map,
+// Scores kernel on the fp8 key cache (e4m3 codes + per-key fp32 scale in
+// p.key_scales): the codes feed tcgen05.mma kind::f8f6f4 directly, against
+// each query split into two e4m3 terms in the kernel.  qraw_map: bf16
+// queries, unswizzled; w_map: head weights.
+cudaError_t launch_scores_fp8(const CUtensorMap& codes_map, const CUtensorMap& qraw_map, const CUtensorMap& w_map,
                               const ScoresParams& p, cudaStream_t stream);
 
 // Top-k kernel: one CTA per request row, radix select over live positions.

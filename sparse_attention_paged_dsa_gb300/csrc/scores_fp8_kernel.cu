@@ -6,27 +6,48 @@
 // k[t, d] = scale[t] * e4m3(code[t, d]).  The deployment on the pages keeps
 // an fp8 KV cache ("The Indexer O(max_context) Breakthrough", section "The
 // Indexer O(max_context) Breakthrough"); the scale format is not given there
-// and is this library's choice.  Because the scale is positive,
-// relu(scale * x) = scale * relu(x), so it is applied once per key after the
-// head sum.  A key costs 68 bytes instead of 128.
+// and is this library's choice.  A key costs 68 bytes instead of 128.
+//
+// The key codes go from HBM to shared memory by TMA and from there straight
+// into tcgen05.mma kind::f8f6f4 (no conversion pass over the keys).  The MMA
+// wants both operands in 8-bit formats, so each bf16 query head is written as
+// an exact sum of two e4m3 terms under a per-head power-of-two scale S_h:
+//     q_h / S_h = hi_h + lo_h / 16,   hi_h = e4m3(q_h / S_h),
+//     lo_h = e4m3(16 * (q_h / S_h - hi_h)),
+// with S_h = 2^(e_h - 7), e_h the binary exponent of max_d |q_h,d|.  A bf16
+// value carries 8 significant bits; hi keeps the top 4 (rounded) and the
+// rounding remainder is a multiple of the value's last bit no larger than
+// 8 of them, which e4m3 holds exactly.  So every element within 2^13 of its
+// head's largest one is represented exactly; smaller ones keep an absolute
+// error below 2^-14 of the head's largest element.  The 32 heads become
+// N = 64 MMA rows (hi and lo of head h at rows 2h and 2h+1), and
+//     q_h . k_t = S_h * scale_t * (acc[2h] + acc[2h+1] / 16)
+// where acc is the fp32 accumulator over the e4m3 codes.  S_h and scale_t
+// are positive, so relu commutes with them: the epilogue forms
+// w_h * S_h * relu(acc[2h] + acc[2h+1] / 16), sums over heads and multiplies
+// by scale_t once.
 //
 // Pipeline (per CTA, two CTAs per SM, persistent grid sized by the device):
-//   * warp 0: the unit schedule and page ids of scores_common.cuh; per unit
-//     two 4 KiB TMA code boxes and two 256 B scale boxes into a raw ring;
-//     query tiles into a 2-slot ring; unit metadata into a ring.
-//   * warps 2-5 (converters): widen the 128 x 64 codes to bf16 (exact: every
-//     e4m3 value is a bf16 value) straight into the 128-byte-swizzled K-major
-//     tile the MMA reads, copy the 128 scales to a scale ring, release the
-//     raw stage, fence the async proxy and publish the tile.
-//   * warp 1: tcgen05.mma kind::f16 M=128 x N=32 x K=64 into one of 4 TMEM
-//     accumulators, as in the bf16 kernel.
-//   * warps 6-9: tcgen05.ld, relu, head weights and head sum in registers,
-//     times the key's scale, live mask, 128-byte stores; the -inf fill of the
-//     dead tail of every row when a full row is requested.
+//   * warp 0: the unit schedule and page ids (scores_common.cuh), staged per
+//     batch in shared memory; lane 0 then issues, per unit, two 4 KiB TMA
+//     code boxes (64-byte swizzle) into an 8-stage ring and posts the unit's
+//     page ids to the scale copier; per request change it stages the bf16
+//     query and its head weights (TMA) for the splitter.
+//   * warp 3: copies each unit's 2 x 256 B of scales into a scale ring with
+//     16-byte cp.async from its 32 lanes, which arrive on the stage's full
+//     barrier (a TMA instruction costs about as much issue time as a whole
+//     page, so the small scale rows do not go through TMA).
+//   * warp 2: per request change, splits the query into the hi/lo e4m3 tile
+//     the MMA reads (64-byte swizzle) and w_h * S_h, in a 4-slot ring that
+//     the epilogue frees when it leaves the request.
+//   * warp 1: tcgen05.mma kind::f8f6f4, M=128 keys x N=64 x K=32, two per
+//     unit, into one of 4 TMEM accumulators of 64 columns.
+//   * warps 4-7: tcgen05.ld, the hi/lo combination, relu, weighted head sum,
+//     key scale, live mask, 128-byte stores; first the -inf fill of the dead
+//     tail of every row when a full row is requested.
 //   * Every wait is bounded (about 1 s); a timeout sets an error bit, stops
 //     all roles, drains in-flight copies and MMAs and frees TMEM.
 #include <cuda.h>
-#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -41,67 +62,107 @@ namespace {
 
 using namespace scores;
 
-constexpr int kRawStages = 3;
-constexpr int kATiles = 3;
-constexpr int kQSlots = 2;
-constexpr int kAccStages = 4;
-constexpr int kMetaRing = 16;  // >= kRawStages + kATiles + kAccStages + 1
-constexpr int kCtasPerSm = 2;
-constexpr int kAccCols = 32;
+// Three CTAs per SM: one TMA-issuing thread keeps too few 4 KiB boxes in
+// flight to cover HBM latency, so the SM runs three independent pipelines.
+constexpr int kStages = 4;       // key-code stages of 8 KiB (two pages)
+constexpr int kQRaw = 2;         // staged bf16 query rows
+constexpr int kQSlots = 2;       // split e4m3 query tiles
+constexpr int kAccStages = 2;
+constexpr int kRing = 8;         // metadata and scale ring, >= kStages + kAccStages + 1
+constexpr int kCtasPerSm = 3;
+constexpr int kAccCols = 64;     // N = 2 x 32 heads
 constexpr uint32_t kTmemCols = kAccStages * kAccCols;  // 128
-constexpr int kConvThreads = 128;
+constexpr int kConvThreads = 32;
 constexpr int kEpiThreads = 128;
-constexpr int kThreads = 64 + kConvThreads + kEpiThreads;  // 320
-constexpr int kATileBytes = 2 * kPageBytes;                 // 16 KiB of bf16: 128 keys x 128 B
-constexpr int kRawBytes = 9216;                             // 2 x 4 KiB codes + 2 x 256 B scales, 1 KiB aligned
-constexpr int kRawScaleOffset = 2 * kPageCodeBytes;
-constexpr uint32_t kIdesc = idesc_bf16_f32(128, kAccCols);
-static_assert(kMetaRing >= kRawStages + kATiles + kAccStages + 1, "metadata ring too small");
-static_assert(kRawScaleOffset + 2 * kPageScaleBytes <= kRawBytes, "raw stage layout");
+constexpr int kThreads = 128 + kEpiThreads;                // producer, MMA, splitter, scale copier, epilogue
+constexpr int kStageBytes = 2 * kPageCodeBytes;            // 8 KiB: 128 keys x 64 B
+constexpr int kQ8Bytes = 2 * kHeads * kHeadDim;            // 4 KiB: 64 rows x 64 B
+constexpr int kUnitScaleBytes = 2 * kPageScaleBytes;       // 512 B
+constexpr int kWRowBytes = kHeads * 4;                     // 128 B
+constexpr uint32_t kFullArrivals = 1 + 32;                 // producer lane 0 + the copier's 32 lanes
+constexpr uint32_t kIdesc = idesc_e4m3_f32(128, kAccCols);
+static_assert(kRing >= kStages + kAccStages + 1, "metadata ring too small");
+static_assert(kTmemCols * kCtasPerSm <= 512, "TMEM columns per SM");
 
-struct __align__(8) SmemCtl {
-    uint64_t rfull[kRawStages];
-    uint64_t rempty[kRawStages];
-    uint64_t afull[kATiles];
-    uint64_t aempty[kATiles];
-    uint64_t qfull[kQSlots];
-    uint64_t qempty[kQSlots];
+struct __align__(16) SmemCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t qraw_full[kQRaw];
+    uint64_t qraw_empty[kQRaw];
+    uint64_t q8_full[kQSlots];
+    uint64_t q8_empty[kQSlots];
     uint64_t tfull[kAccStages];
     uint64_t tempty[kAccStages];
     uint64_t tmeta[kAccStages];
     uint64_t drain;
+    uint64_t unit_posted[kRing];  // a unit's metadata and page ids are readable (scale copier)
     uint32_t tmem_base;
     int abort;
-    int32_t meta[kMetaRing];
-    float scale[kMetaRing][128];  // the unit's 128 key scales, by unit sequence number
+    int32_t meta[kRing];
+    int2 unit_pages[kRing];       // valid page ids of each unit (-1: none)
+    int4 batch_units[kBatch];     // the producer's current batch: request, pair, page ids
+    int32_t qrow[kQRaw];                      // request of each staged query (-1: no more)
+    __align__(16) float wq[kQSlots][kHeads];  // w_h * S_h of each split query
     RowTable rows;
 };
 
-constexpr size_t kTileBytes = size_t(kATiles) * kATileBytes + size_t(kQSlots) * kQRowBytes +
-                              size_t(kRawStages) * kRawBytes;
+// Tile region (1024-byte aligned base): stages | q8 slots | raw queries | scales | raw weights.
+constexpr size_t kOffQ8 = size_t(kStages) * kStageBytes;
+constexpr size_t kOffQRaw = kOffQ8 + size_t(kQSlots) * kQ8Bytes;
+constexpr size_t kOffScales = kOffQRaw + size_t(kQRaw) * kQRowBytes;
+constexpr size_t kOffWRaw = kOffScales + size_t(kRing) * kUnitScaleBytes;
+constexpr size_t kTileBytes = kOffWRaw + size_t(kQRaw) * kWRowBytes;
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes + sizeof(SmemCtl);
-static_assert(kSmemBytes * kCtasPerSm <= 228 * 1024, "shared memory budget per SM");
+static_assert(kTileBytes % 16 == 0, "control block alignment");
+static_assert(kSmemBytes * kCtasPerSm <= 226 * 1024, "shared memory budget per SM");
 
-// Four e4m3 codes (lowest byte first) to four bf16 values, exactly.
-__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t codes) {
-    uint32_t h01, h23;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(static_cast<unsigned short>(codes & 0xFFFFu)));
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(static_cast<unsigned short>(codes >> 16)));
-    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-    const __nv_bfloat162 b01 = __float22bfloat162_rn(f01);
-    const __nv_bfloat162 b23 = __float22bfloat162_rn(f23);
-    return make_uint2(*reinterpret_cast<const uint32_t*>(&b01), *reinterpret_cast<const uint32_t*>(&b23));
+// 16-byte global -> shared copy through L2 only (cp.async), and the arrival on
+// `bar` that fires once all of this thread's earlier cp.async copies landed
+// (counted in the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Two floats to two e4m3 codes (round to nearest even, saturating); `lo_val` in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo_val, float hi_val) {
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi_val), "f"(lo_val));
+    return r;
+}
+
+// Two e4m3 codes (low byte first) to two floats, exactly.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t codes) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<unsigned short>(codes & 0xFFFFu)));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Split 8 consecutive query values (already divided by S_h) into 8 hi and 8 lo codes.
+__device__ __forceinline__ void split8(const float* x, uint2& hi, uint2& lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        h[i] = f32x2_to_e4m3x2(x[2 * i], x[2 * i + 1]);
+        const float2 hv = e4m3x2_to_f32x2(h[i]);
+        l[i] = f32x2_to_e4m3x2(16.f * (x[2 * i] - hv.x), 16.f * (x[2 * i + 1] - hv.y));
+    }
+    hi = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    lo = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    scores_fp8_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap scales_map,
-                      const __grid_constant__ CUtensorMap q_map, const ScoresParams p) {
+    scores_fp8_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap qraw_map,
+                      const __grid_constant__ CUtensorMap w_map, const ScoresParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* atiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* qtiles = atiles + size_t(kATiles) * kATileBytes;
-    uint8_t* raw = qtiles + size_t(kQSlots) * kQRowBytes;
-    SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(atiles + kTileBytes);
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* q8 = tiles + kOffQ8;
+    uint8_t* qraw = tiles + kOffQRaw;
+    const float* scale_ring = reinterpret_cast<const float*>(tiles + kOffScales);
+    const float* wraw = reinterpret_cast<const float*>(tiles + kOffWRaw);
+    SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(tiles + kTileBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -109,17 +170,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     // ---- set-up that touches no global memory (overlaps the previous kernel).
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kRawStages; ++s) {
-            mbar_init(&ctl.rfull[s], 1);
-            mbar_init(&ctl.rempty[s], kConvThreads);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ctl.full[s], kFullArrivals);
+            mbar_init(&ctl.empty[s], 1);
         }
-        for (int s = 0; s < kATiles; ++s) {
-            mbar_init(&ctl.afull[s], kConvThreads);
-            mbar_init(&ctl.aempty[s], 1);
+        for (int s = 0; s < kQRaw; ++s) {
+            mbar_init(&ctl.qraw_full[s], 1);
+            mbar_init(&ctl.qraw_empty[s], kConvThreads);
         }
         for (int s = 0; s < kQSlots; ++s) {
-            mbar_init(&ctl.qfull[s], 1);
-            mbar_init(&ctl.qempty[s], 1);
+            mbar_init(&ctl.q8_full[s], kConvThreads);
+            mbar_init(&ctl.q8_empty[s], kEpiThreads / 32);
         }
         for (int a = 0; a < kAccStages; ++a) {
             mbar_init(&ctl.tfull[a], 1);
@@ -127,11 +188,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             mbar_init(&ctl.tmeta[a], 1);
         }
         mbar_init(&ctl.drain, 1);
+        for (int r = 0; r < kRing; ++r) mbar_init(&ctl.unit_posted[r], 1);
         ctl.abort = 0;
         fence_mbar_init();
         tma_prefetch_map(&codes_map);
-        tma_prefetch_map(&scales_map);
-        tma_prefetch_map(&q_map);
+        tma_prefetch_map(&qraw_map);
+        tma_prefetch_map(&w_map);
     }
     if (warp == 1) {
         tmem_alloc(&ctl.tmem_base, kTmemCols);
@@ -149,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int64_t M = p.row_width;
 
     if (warp == 0) {
-        // ================= producer: schedule, page ids, TMA of codes and scales =================
+        // ================= producer: schedule, page ids, TMA of codes, scales, queries =================
         const uint64_t pol_keys = l2_policy_evict_first();
         const uint64_t pol_q = l2_policy_evict_last();
         int stage = 0, issued = 0, q_issued = 0, q_row = -1, seq = 0;
@@ -160,83 +222,86 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         sched.next(cur_u0, cur_cnt, lane);
         UnitPrep cur = prepare_units(ctl.rows, p, cur_u0, cur_cnt, lane);
         while (cur_cnt > 0 && !stop) {
+            if (lane < cur_cnt) ctl.batch_units[lane] = make_int4(cur.b, cur.pair, cur.pg0, cur.pg1);
+            __syncwarp();
             int nxt_u0, nxt_cnt;
             sched.next(nxt_u0, nxt_cnt, lane);
             const UnitPrep nxt = prepare_units(ctl.rows, p, nxt_u0, nxt_cnt, lane);  // loads in flight
-            for (int i = 0; i < cur_cnt; ++i) {
-                const int bi = __shfl_sync(0xffffffffu, cur.b, i);
-                const int pi = __shfl_sync(0xffffffffu, cur.pair, i);
-                const int g0 = __shfl_sync(0xffffffffu, cur.pg0, i);
-                const int g1 = __shfl_sync(0xffffffffu, cur.pg1, i);
-                int failed = 0;
-                if (lane == 0) {
-                    if (bi != q_row) {
-                        const int qs = q_issued % kQSlots;
-                        if (!mbar_wait(&ctl.qempty[qs], ((q_issued / kQSlots) & 1) ^ 1u, &ctl.abort)) {
+            int failed = 0;
+            if (lane == 0) {
+                for (int i = 0; i < cur_cnt; ++i) {
+                    const int4 un = ctl.batch_units[i];
+                    const int bi = un.x, g0 = un.z, g1 = un.w;
+                    if (bi != q_row) {  // new request: stage its query and head weights for the splitter
+                        const int qs = q_issued % kQRaw;
+                        if (!mbar_wait(&ctl.qraw_empty[qs], ((q_issued / kQRaw) & 1) ^ 1u, &ctl.abort)) {
                             failed = 1;
-                        } else {
-                            mbar_arrive_expect_tx(&ctl.qfull[qs], kQRowBytes);
-                            tma_load_2d(qtiles + size_t(qs) * kQRowBytes, &q_map, &ctl.qfull[qs], 0, bi * kHeads,
-                                        pol_q);
-                            ++q_issued;
-                            q_row = bi;
+                            break;
                         }
+                        ctl.qrow[qs] = bi;
+                        mbar_arrive_expect_tx(&ctl.qraw_full[qs], kQRowBytes + kWRowBytes);
+                        tma_load_2d(qraw + size_t(qs) * kQRowBytes, &qraw_map, &ctl.qraw_full[qs], 0, bi * kHeads,
+                                    pol_q);
+                        tma_load_2d(tiles + kOffWRaw + size_t(qs) * kWRowBytes, &w_map, &ctl.qraw_full[qs], 0, bi,
+                                    pol_q);
+                        ++q_issued;
+                        q_row = bi;
                     }
-                    if (!failed && !mbar_wait(&ctl.rempty[stage], phase ^ 1u, &ctl.abort)) failed = 1;
-                    if (!failed) {
-                        const bool ok0 = g0 >= 0 && g0 < p.num_pages;
-                        const bool ok1 = g1 >= 0 && g1 < p.num_pages;
-                        if (!ok0 || (g1 != -2 && !ok1)) atomicOr(p.err, kErrBadPage);
-                        ctl.meta[seq % kMetaRing] = pack_meta(bi, pi, ok0, ok1);
-                        const uint32_t bytes = (ok0 ? kPageCodeBytes + kPageScaleBytes : 0) +
-                                               (ok1 ? kPageCodeBytes + kPageScaleBytes : 0);
-                        uint8_t* r = raw + size_t(stage) * kRawBytes;
-                        if (bytes != 0) {
-                            mbar_arrive_expect_tx(&ctl.rfull[stage], bytes);
-                            if (ok0) {
-                                tma_load_3d(r, &codes_map, &ctl.rfull[stage], 0, 0, g0, pol_keys);
-                                tma_load_2d(r + kRawScaleOffset, &scales_map, &ctl.rfull[stage], 0, g0, pol_keys);
-                            }
-                            if (ok1) {
-                                tma_load_3d(r + kPageCodeBytes, &codes_map, &ctl.rfull[stage], 0, 0, g1, pol_keys);
-                                tma_load_2d(r + kRawScaleOffset + kPageScaleBytes, &scales_map, &ctl.rfull[stage], 0,
-                                            g1, pol_keys);
-                            }
-                        } else {
-                            mbar_arrive(&ctl.rfull[stage]);  // nothing to load
-                        }
-                        ++issued;
+                    if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort)) {
+                        failed = 1;
+                        break;
                     }
-                }
-                if (__shfl_sync(0xffffffffu, failed, 0)) {
-                    stop = true;
-                    break;
-                }
-                ++seq;
-                if (++stage == kRawStages) {
-                    stage = 0;
-                    phase ^= 1u;
+                    const bool ok0 = g0 >= 0 && g0 < p.num_pages;
+                    const bool ok1 = g1 >= 0 && g1 < p.num_pages;
+                    if (!ok0 || (g1 != -2 && !ok1)) atomicOr(p.err, kErrBadPage);
+                    ctl.meta[seq % kRing] = pack_meta(bi, un.y, ok0, ok1);
+                    ctl.unit_pages[seq % kRing] = make_int2(ok0 ? g0 : -1, ok1 ? g1 : -1);
+                    mbar_arrive(&ctl.unit_posted[seq % kRing]);
+                    const uint32_t bytes = (ok0 ? kPageCodeBytes : 0) + (ok1 ? kPageCodeBytes : 0);
+                    uint8_t* a = tiles + size_t(stage) * kStageBytes;
+                    if (bytes != 0) {
+                        mbar_arrive_expect_tx(&ctl.full[stage], bytes);
+                        if (ok0) tma_load_3d(a, &codes_map, &ctl.full[stage], 0, 0, g0, pol_keys);
+                        if (ok1) tma_load_3d(a + kPageCodeBytes, &codes_map, &ctl.full[stage], 0, 0, g1, pol_keys);
+                    } else {
+                        mbar_arrive(&ctl.full[stage]);  // nothing to load
+                    }
+                    ++issued;
+                    ++seq;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
+            __syncwarp();
+            stop = __shfl_sync(0xffffffffu, failed, 0) != 0;
+            seq = __shfl_sync(0xffffffffu, seq, 0);
+            stage = __shfl_sync(0xffffffffu, stage, 0);
+            phase = __shfl_sync(0xffffffffu, phase, 0);
+            issued = __shfl_sync(0xffffffffu, issued, 0);
+            q_issued = __shfl_sync(0xffffffffu, q_issued, 0);
+            q_row = __shfl_sync(0xffffffffu, q_row, 0);
             cur_u0 = nxt_u0;
             cur_cnt = nxt_cnt;
             cur = nxt;
         }
-        if (!stop) {  // end-of-work marker
+        if (!stop) {  // end-of-work markers: one for the splitters, one for the MMA issuer and epilogue
             int failed = 0;
             if (lane == 0) {
-                if (!mbar_wait(&ctl.rempty[stage], phase ^ 1u, &ctl.abort)) {
+                const int qs = q_issued % kQRaw;
+                if (!mbar_wait(&ctl.qraw_empty[qs], ((q_issued / kQRaw) & 1) ^ 1u, &ctl.abort) ||
+                    !mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort)) {
                     failed = 1;
                 } else {
-                    ctl.meta[seq % kMetaRing] = kEndOfWork;
-                    mbar_arrive(&ctl.rfull[stage]);
+                    ctl.qrow[qs] = -1;
+                    mbar_arrive(&ctl.qraw_full[qs]);
+                    ctl.meta[seq % kRing] = kEndOfWork;
+                    mbar_arrive(&ctl.unit_posted[seq % kRing]);
+                    mbar_arrive(&ctl.full[stage]);
                 }
             }
             if (__shfl_sync(0xffffffffu, failed, 0)) stop = true;
-            if (++stage == kRawStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
         }
         if (lane == 0 && stop) {
             atomicOr(p.err, kErrWaitTimeout);
@@ -245,58 +310,57 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (lane == 0 && ctl.abort) {  // let every copy this CTA issued land before it may exit
             int s = stage;
             uint32_t ph = phase;
-            for (int i = 0; i < min(issued, kRawStages); ++i) {
+            for (int i = 0; i < min(issued, kStages); ++i) {
                 if (s == 0) {
-                    s = kRawStages - 1;
+                    s = kStages - 1;
                     ph ^= 1u;
                 } else {
                     --s;
                 }
-                wait_landed(&ctl.rfull[s], ph);
+                wait_landed(&ctl.full[s], ph);
             }
-            for (int j = max(0, q_issued - kQSlots); j < q_issued; ++j)
-                wait_landed(&ctl.qfull[j % kQSlots], (j / kQSlots) & 1);
+            for (int j = max(0, q_issued - kQRaw); j < q_issued; ++j)
+                wait_landed(&ctl.qraw_full[j % kQRaw], (j / kQRaw) & 1);
         }
     } else if (warp == 1) {
         // ================= MMA issuer (one lane) =================
         if (lane == 0) {
-            int as = 0, acc = 0, seq = 0, q_row = -1, q_used = -1;
-            uint32_t aphase = 0, acc_phase = 0;
+            int stage = 0, acc = 0, seq = 0, q_row = -1, q_used = -1;
+            uint32_t phase = 0, acc_phase = 0;
             bool stop = false;
             while (true) {
-                if (!mbar_wait(&ctl.afull[as], aphase, &ctl.abort) ||
+                if (!mbar_wait(&ctl.full[stage], phase, &ctl.abort) ||
                     !mbar_wait(&ctl.tempty[acc], acc_phase ^ 1u, &ctl.abort)) {
                     stop = true;
                     break;
                 }
-                const int m = ctl.meta[seq % kMetaRing];
+                const int m = ctl.meta[seq % kRing];
                 if (m != kEndOfWork) {
                     const int b = meta_row(m);
                     if (b != q_row) {
-                        if (q_used >= 0) umma_commit(&ctl.qempty[q_used % kQSlots]);
                         ++q_used;
                         q_row = b;
-                        if (!mbar_wait(&ctl.qfull[q_used % kQSlots], (q_used / kQSlots) & 1, &ctl.abort)) {
+                        if (!mbar_wait(&ctl.q8_full[q_used % kQSlots], (q_used / kQSlots) & 1, &ctl.abort)) {
                             stop = true;
                             break;
                         }
                     }
                     tc_fence_after_sync();
-                    const uint64_t a_desc = smem_desc_kmajor_sw128(smem_u32(atiles + size_t(as) * kATileBytes));
+                    const uint64_t a_desc = smem_desc_kmajor_sw64(smem_u32(tiles + size_t(stage) * kStageBytes));
                     const uint64_t b_desc =
-                        smem_desc_kmajor_sw128(smem_u32(qtiles + size_t(q_used % kQSlots) * kQRowBytes));
+                        smem_desc_kmajor_sw64(smem_u32(q8 + size_t(q_used % kQSlots) * kQ8Bytes));
                     const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
 #pragma unroll
-                    for (int kk = 0; kk < kHeadDim / 16; ++kk)
-                        umma_bf16_ss(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, kIdesc, kk > 0 ? 1u : 0u);
-                    umma_commit(&ctl.aempty[as]);
+                    for (int kk = 0; kk < kHeadDim / 32; ++kk)  // K = 32 codes per MMA: +32 bytes = +2 in the address field
+                        umma_f8_ss(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, kIdesc, kk > 0 ? 1u : 0u);
+                    umma_commit(&ctl.empty[stage]);
                     umma_commit(&ctl.tfull[acc]);
                 }
                 mbar_arrive(&ctl.tmeta[acc]);
                 ++seq;
-                if (++as == kATiles) {
-                    as = 0;
-                    aphase ^= 1u;
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
                 if (++acc == kAccStages) {
                     acc = 0;
@@ -312,67 +376,102 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             wait_landed(&ctl.drain, 0);
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // ================= converters: e4m3 codes -> bf16 swizzled tile, scales =================
-        const int ct = threadIdx.x - 64;  // 0..127
-        const int cw = warp - 2;          // rows [32 cw, 32 cw + 32)
-        const int half = lane >> 4;       // which of the two rows of an iteration
-        const int col4 = lane & 15;       // codes [4 col4, 4 col4 + 4) of the row
-        int rs = 0, as = 0, seq = 0;
-        uint32_t rphase = 0, aphase = 0;
+    } else if (warp == 2) {
+        // ================= query splitter: bf16 q -> hi/lo e4m3 tile and w_h * S_h =================
+        const int h = lane;  // head
         bool stop = false;
-        while (true) {
-            if (!mbar_wait(&ctl.rfull[rs], rphase, &ctl.abort) ||
-                !mbar_wait(&ctl.aempty[as], aphase ^ 1u, &ctl.abort)) {
+        for (int j = 0;; ++j) {
+            const int rs = j % kQRaw;
+            if (!mbar_wait(&ctl.qraw_full[rs], (j / kQRaw) & 1, &ctl.abort)) {
                 stop = true;
                 break;
             }
-            const int m = ctl.meta[seq % kMetaRing];
-            if (m != kEndOfWork) {
-                const uint8_t* r = raw + size_t(rs) * kRawBytes;
-                uint8_t* tile = atiles + size_t(as) * kATileBytes;
-#pragma unroll 4
-                for (int it = 0; it < 16; ++it) {
-                    const int row = 32 * cw + 2 * it + half;  // key row of the unit: page row >> 6, entry row & 63
-                    const uint32_t codes =
-                        *reinterpret_cast<const uint32_t*>(r + (row >> 6) * kPageCodeBytes + (row & 63) * kHeadDim +
-                                                           4 * col4);
-                    const uint2 v = e4m3x4_to_bf16x4(codes);
-                    *reinterpret_cast<uint2*>(tile + row * 128 + (((col4 >> 1) ^ (row & 7)) << 4) + ((col4 & 1) << 3)) =
-                        v;
+            if (ctl.qrow[rs] < 0) break;
+            const int qs = j % kQSlots;
+            if (!mbar_wait(&ctl.q8_empty[qs], ((j / kQSlots) & 1) ^ 1u, &ctl.abort)) {
+                stop = true;
+                break;
+            }
+            const uint4* src = reinterpret_cast<const uint4*>(qraw + size_t(rs) * kQRowBytes + h * 128);
+            uint32_t amax_bits = 0;  // max |q| over the head, on the bf16 magnitude bits
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint4 u = src[v];
+                const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    amax_bits = max(amax_bits, max(wds[i] & 0x7FFFu, (wds[i] >> 16) & 0x7FFFu));
+            }
+            // S_h = 2^(e - 7) with e the exponent of the head's largest magnitude (clamped so
+            // that S_h and 1 / S_h are normal floats); all-zero heads take e = 0.
+            int e = amax_bits != 0 ? int(amax_bits >> 7) - 127 : 0;
+            e = max(e, -119);
+            const float inv_s = __uint_as_float(uint32_t(127 + 7 - e) << 23);
+            const float s_h = __uint_as_float(uint32_t(127 + e - 7) << 23);
+            uint8_t* tile = q8 + size_t(qs) * kQ8Bytes;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {  // 16-byte chunk c of rows 2h (hi) and 2h + 1 (lo)
+                float x[16];
+#pragma unroll
+                for (int v = 0; v < 2; ++v) {
+                    const uint4 u = src[2 * c + v];
+                    const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        x[8 * v + 2 * i] = __uint_as_float(wds[i] << 16) * inv_s;
+                        x[8 * v + 2 * i + 1] = __uint_as_float(wds[i] & 0xFFFF0000u) * inv_s;
+                    }
                 }
-                ctl.scale[seq % kMetaRing][ct] =
-                    *reinterpret_cast<const float*>(r + kRawScaleOffset + (ct >> 6) * kPageScaleBytes + (ct & 63) * 4);
+                uint2 hi0, lo0, hi1, lo1;
+                split8(x, hi0, lo0);
+                split8(x + 8, hi1, lo1);
+                const int sw = (c ^ (h & 3)) << 4;  // 64-byte swizzle: rows 2h, 2h+1 share (row >> 1) & 3
+                *reinterpret_cast<uint4*>(tile + (2 * h) * 64 + sw) = make_uint4(hi0.x, hi0.y, hi1.x, hi1.y);
+                *reinterpret_cast<uint4*>(tile + (2 * h + 1) * 64 + sw) = make_uint4(lo0.x, lo0.y, lo1.x, lo1.y);
             }
-            mbar_arrive(&ctl.rempty[rs]);
+            ctl.wq[qs][h] = wraw[rs * kHeads + h] * s_h;
+            mbar_arrive(&ctl.qraw_empty[rs]);
             fence_proxy_async_smem();
-            mbar_arrive(&ctl.afull[as]);
-            ++seq;
-            if (++rs == kRawStages) {
-                rs = 0;
-                rphase ^= 1u;
-            }
-            if (++as == kATiles) {
-                as = 0;
-                aphase ^= 1u;
-            }
-            if (m == kEndOfWork) break;
+            mbar_arrive(&ctl.q8_full[qs]);
         }
         if (stop && lane == 0) {
             atomicOr(p.err, kErrWaitTimeout);
             ctl.abort = 1;
         }
+    } else if (warp == 3) {
+        // ================= scale copier: 2 x 256 B of key scales per unit =================
+        bool stop = false;
+        for (int seq = 0;; ++seq) {
+            const int r = seq % kRing;
+            if (!mbar_wait(&ctl.unit_posted[r], (seq / kRing) & 1, &ctl.abort)) {
+                stop = true;
+                break;
+            }
+            const bool end = ctl.meta[r] == kEndOfWork;
+            if (!end) {  // lane l: page l / 16, entries 4 (l % 16) .. + 3
+                const int2 pg = ctl.unit_pages[r];
+                const int g = lane < 16 ? pg.x : pg.y;
+                if (g >= 0)
+                    cp_async_16(tiles + kOffScales + size_t(r) * kUnitScaleBytes + lane * 16,
+                                p.key_scales + int64_t(g) * kPageEntries + (lane & 15) * 4);
+            }
+            cp_async_arrive_noinc(&ctl.full[seq % kStages]);
+            if (end) break;
+        }
+        if (stop && lane == 0) {
+            atomicOr(p.err, kErrWaitTimeout);
+            ctl.abort = 1;
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");  // no scale copy outlives the CTA
     } else {
-        // ================= epilogue: warps 6..9 =================
-        const int et = threadIdx.x - 192;  // 0..127
+        // ================= epilogue: warps 4..7 =================
+        const int et = threadIdx.x - 128;  // 0..127
         const int quad = warp & 3;         // TMEM lanes [32*quad, 32*quad + 32)
         const float neg_inf = __int_as_float(0xff800000);
         if (p.fill_dead) fill_dead_tails(ctl.rows, p, et, kEpiThreads);
 
-        int cur_b = -1, n = 0;
-        float wv[kHeads];
-#pragma unroll
-        for (int h = 0; h < kHeads; ++h) wv[h] = 0.f;
+        int cur_b = -1, n = 0, q_used = -1;
+        const float* wv = ctl.wq[0];  // w_h * S_h of the current request (shared memory)
         bool stop = false;
         for (int i = 0;; ++i) {
             const int acc = i % kAccStages;
@@ -381,22 +480,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 stop = true;
                 break;
             }
-            const int m = ctl.meta[i % kMetaRing];
+            const int m = ctl.meta[i % kRing];
             if (m == kEndOfWork) break;
             const int b = meta_row(m);
             const int pair = meta_pair(m);
             const bool page_ok = (m >> (quad >> 1)) & 1;
-            const float key_scale = ctl.scale[i % kMetaRing][quad * 32 + lane];
+            const float key_scale = scale_ring[(i % kRing) * (kUnitScaleBytes / 4) + quad * 32 + lane];
             if (b != cur_b) {
-                const float4* wr = reinterpret_cast<const float4*>(p.w + int64_t(b) * kHeads);
-#pragma unroll
-                for (int h4 = 0; h4 < kHeads / 4; ++h4) {
-                    const float4 v = __ldg(wr + h4);
-                    wv[4 * h4 + 0] = v.x;
-                    wv[4 * h4 + 1] = v.y;
-                    wv[4 * h4 + 2] = v.z;
-                    wv[4 * h4 + 3] = v.w;
-                }
+                if (q_used >= 0 && lane == 0) mbar_arrive(&ctl.q8_empty[q_used % kQSlots]);  // done with that query
+                ++q_used;
+                wv = ctl.wq[q_used % kQSlots];
                 n = ctl.rows.n_live[b];
                 cur_b = b;
             }
@@ -405,19 +498,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 break;
             }
             tc_fence_after_sync();
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * kAccCols), r);
-            tmem_ld_wait(r);
-            tc_fence_before_sync();
-            mbar_arrive(&ctl.tempty[acc]);
-
+            const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * kAccCols);
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr, r);  // heads 0-15: hi, lo interleaved
+                tmem_ld_wait(r);
 #pragma unroll
-            for (int h = 0; h < kHeads; h += 4) {
-                s0 = fmaf(wv[h + 0], fmaxf(__uint_as_float(r[h + 0]), 0.f), s0);
-                s1 = fmaf(wv[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
-                s2 = fmaf(wv[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
-                s3 = fmaf(wv[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
+                for (int h = 0; h < 16; h += 2) {
+                    const float d0 = fmaf(__uint_as_float(r[2 * h + 1]), 0.0625f, __uint_as_float(r[2 * h]));
+                    const float d1 = fmaf(__uint_as_float(r[2 * h + 3]), 0.0625f, __uint_as_float(r[2 * h + 2]));
+                    s0 = fmaf(wv[h], fmaxf(d0, 0.f), s0);
+                    s1 = fmaf(wv[h + 1], fmaxf(d1, 0.f), s1);
+                }
+            }
+            {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + 32, r);  // heads 16-31
+                tmem_ld_wait(r);
+                tc_fence_before_sync();
+                mbar_arrive(&ctl.tempty[acc]);
+#pragma unroll
+                for (int h = 0; h < 16; h += 2) {
+                    const float d2 = fmaf(__uint_as_float(r[2 * h + 1]), 0.0625f, __uint_as_float(r[2 * h]));
+                    const float d3 = fmaf(__uint_as_float(r[2 * h + 3]), 0.0625f, __uint_as_float(r[2 * h + 2]));
+                    s2 = fmaf(wv[16 + h], fmaxf(d2, 0.f), s2);
+                    s3 = fmaf(wv[17 + h], fmaxf(d3, 0.f), s3);
+                }
             }
             const float s = key_scale * ((s0 + s1) + (s2 + s3));
             const int64_t t = int64_t(pair) * kUnitPositions + quad * 32 + lane;
@@ -440,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 }  // namespace
 
-cudaError_t launch_scores_fp8(const CUtensorMap& codes_map, const CUtensorMap& scales_map, const CUtensorMap& q_map,
+cudaError_t launch_scores_fp8(const CUtensorMap& codes_map, const CUtensorMap& qraw_map, const CUtensorMap& w_map,
                               const ScoresParams& p, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
@@ -465,7 +572,7 @@ cudaError_t launch_scores_fp8(const CUtensorMap& codes_map, const CUtensorMap& s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, scores_fp8_kernel, codes_map, scales_map, q_map, p);
+    return cudaLaunchKernelEx(&cfg, scores_fp8_kernel, codes_map, qraw_map, w_map, p);
 }
 
 }  // namespace dsa

@@ -57,10 +57,12 @@ namespace {
 
 using namespace scores;
 
-constexpr int kStages = 4;                             // 16 KiB stages per CTA
-constexpr int kEpiGroups = 2;                          // epilogue groups of 4 warps
-constexpr int kCtasPerSm = 2;                          // two independent pipelines per SM
-constexpr int kQSlots = 4;
+// Three CTAs per SM: one TMA-issuing thread keeps too few page boxes in
+// flight to cover HBM latency, so the SM runs three independent pipelines.
+constexpr int kStages = 3;                             // 16 KiB stages per CTA
+constexpr int kEpiGroups = 1;                          // epilogue groups of 4 warps
+constexpr int kCtasPerSm = 3;                          // three independent pipelines per SM
+constexpr int kQSlots = 2;
 constexpr int kAccStages = 4;
 constexpr int kMetaRing = 16;                          // >= kStages + kAccStages + 1
 constexpr int kAccCols = 32;                           // fp32 columns per accumulator (N = 32 heads)
