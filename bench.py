@@ -41,7 +41,11 @@ FP8_KEY_BYTES_PER_POSITION = 68       # 64 e4m3 codes + one fp32 scale (fp8 key 
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 512 << 20               # > 2x the 129 MB L2
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "scores_kernel_b64_ctx128k_dense.md")
+PROFILE_SUMMARY_FP8 = os.path.join(ROOT, "profiles", "scores_fp8_kernel_b64_ctx128k_dense.md")
 SCORES_SRC = os.path.join(ROOT, "sparse_attention_paged_dsa_gb300", "csrc", "scores_kernel.cu")
+SCORES_FP8_SRC = os.path.join(ROOT, "sparse_attention_paged_dsa_gb300", "csrc", "scores_fp8_kernel.cu")
+SCORES_COMMON_SRC = os.path.join(ROOT, "sparse_attention_paged_dsa_gb300", "csrc", "scores_common.cuh")
+PTX_SRC = os.path.join(ROOT, "sparse_attention_paged_dsa_gb300", "csrc", "sm103_ptx.cuh")
 
 
 def parse_args(argv=None):
@@ -160,13 +164,16 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic():
-    """DRAM bytes per scores launch from the committed ncu summary, if the kernel is unchanged."""
+def profiled_traffic(summary, src):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged since."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(summary).read()
     except OSError:
         return None
-    sha = hashlib.sha256(open(SCORES_SRC, "rb").read()).hexdigest()
+    h = hashlib.sha256()
+    for f in (src, SCORES_COMMON_SRC, PTX_SRC):  # the kernel and the headers it is built from
+        h.update(open(f, "rb").read())
+    sha = h.hexdigest()
     fields = dict(l.split(":", 1) for l in text.splitlines() if l.startswith(("source_sha256:", "dram_bytes_per_launch:")))
     if fields.get("source_sha256", "").strip() != sha:
         return None
@@ -192,6 +199,46 @@ def cpu_baseline(case, rows: int):
     return {"value": pos / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {rows} of {case.batch} rows ({pos} live positions), fp64 scores + full-sort top-k, "
                       f"{dt:.2f} s"}
+
+
+def time_loop(fn, n, stream, flush=None):
+    """CUDA-event time of `n` back-to-back calls of `fn` on `stream`.
+
+    Without `flush`: one event pair around the whole loop (nothing is put between
+    calls, so consecutive launches overlap as they would in a serving loop);
+    returns (mean seconds per call, None).  With `flush` (a callable that
+    evicts L2): events around every call, the flush outside them; returns
+    (mean, per-call list)."""
+    import torch
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / n, None
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        flush()
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) * 1e-3 for a, b in ev]
+    return statistics.fmean(per), per
+
+
+def per_call_events(fn, n, stream):
+    """Per-call CUDA-event times (an event between calls; for percentiles only)."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e-3 for a, b in ev]
 
 
 def graph_us_per_call(fn, reps=20, replays=20):
@@ -267,25 +314,19 @@ def run_fp8(args, case, binding, inputs, device, stream, live):
         scores_only()
     torch.cuda.synchronize(device)
     n = max(10, min(args.steps, 500))
-    out = {}
-    for name, fn in (("step", step), ("scores", scores_only)):
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-        for i in range(n):
-            ev[i][0].record(stream)
-            fn()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize(device)
-        out[name] = [e[0].elapsed_time(e[1]) * 1e-3 for e in ev]
+    t_step, _ = time_loop(step, n, stream)
+    t_scores, _ = time_loop(scores_only, n, stream)
     if binding.get_error(ws) != 0:
         raise RuntimeError("device error word set in the fp8 run")
     peak, peak_kind = measured_hbm_peak()
-    t_step, t_scores = statistics.fmean(out["step"]), statistics.fmean(out["scores"])
+    traffic = profiled_traffic(PROFILE_SUMMARY_FP8, SCORES_FP8_SRC)
     achieved = live * FP8_KEY_BYTES_PER_POSITION / t_scores / 1e9
     return {"value": live / t_step, "unit": UNIT, "steps": n, "ms_per_step": 1e3 * t_step,
             "scores_kernel_us": 1e6 * t_scores,
             "graph_us": {"scores": graph_us_per_call(scores_only), "fused": graph_us_per_call(step)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "kernel": "scores_fp8_kernel", "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
+                         "traffic": traffic, "kernel": "scores_fp8_kernel",
+                         "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
                          "algorithmic_bytes_per_launch": live * FP8_KEY_BYTES_PER_POSITION},
             "cache": "e4m3 codes [pages, 64, 64] + fp32 scale per key (max|k| / 448), made from the bf16 keys",
             "step": "dsa_indexer_fused_fp8 with the full-width scores row"}
@@ -386,39 +427,29 @@ def run_ours(args):
         raise RuntimeError("device error word set during warm-up")
 
     n = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    flush_fn = (lambda: flush.zero_()) if args.l2_flush else None
     with ClockSampler(device.index) as clocks:
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(device)
         clocks.mark_start()
         wall0 = time.perf_counter()
-        for i in range(n):
-            maybe_flush()
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize(device)
+        mean_step, per_step = time_loop(step, n, stream, flush_fn)
         if world > 1:
             dist.barrier()
         wall1 = time.perf_counter()
         clocks.mark_end()
-    t_step = [e[0].elapsed_time(e[1]) * 1e-3 for e in ev]
-    local_seconds = sum(t_step)
-    total_units, max_seconds = aggregate(live * n, local_seconds)
+    total_units, max_seconds = aggregate(live * n, mean_step * n)
     value = total_units / max_seconds
+    if per_step is None:  # percentiles from a separate loop with an event between steps
+        per_step = per_call_events(step, max(10, min(n, 200)), stream)
 
     # The dominant kernel alone: the scores entry point launches the same scores kernel the fused call
-    # launches first; same workload, same L2 flush between launches.
+    # launches first; same workload, same L2 setting between launches.
     n_k = max(10, min(n, 500))
-    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_k)]
-    for i in range(n_k):
-        maybe_flush()
-        evk[i][0].record(stream)
-        scores_only()
-        evk[i][1].record(stream)
-    torch.cuda.synchronize(device)
-    t_scores = [e[0].elapsed_time(e[1]) * 1e-3 for e in evk]
+    mean_scores, per_scores = time_loop(scores_only, n_k, stream, flush_fn)
+    if per_scores is None:
+        per_scores = per_call_events(scores_only, max(10, min(n, 200)), stream)
     if binding.get_error(ws) != 0:
         raise RuntimeError("device error word set during the timed steps")
 
@@ -440,23 +471,27 @@ def run_ours(args):
         return 0
 
     peak, peak_kind = measured_hbm_peak()
-    mean_scores = statistics.fmean(t_scores)
     achieved = live * KEY_BYTES_PER_POSITION / mean_scores / 1e9
-    traffic = profiled_traffic()
+    traffic = profiled_traffic(PROFILE_SUMMARY, SCORES_SRC)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n, "warmup": args.warmup,
-        "ms_per_step": 1e3 * statistics.fmean(t_step), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": 1e3 * mean_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(case, world, args.l2_flush),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "kernel": "scores_kernel",
                      "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
                      "algorithmic_bytes_per_launch": live * KEY_BYTES_PER_POSITION},
-        "kernels_us": {"scores_mean": 1e6 * mean_scores, "scores_median": 1e6 * statistics.median(t_scores),
+        "kernels_us": {"scores_mean": 1e6 * mean_scores,
+                       "scores_median_with_events_between": 1e6 * statistics.median(per_scores),
                        "scores_launches_timed": n_k,
-                       "step_p10": 1e6 * float(np.percentile(t_step, 10)),
-                       "step_p50": 1e6 * float(np.percentile(t_step, 50)),
-                       "step_p90": 1e6 * float(np.percentile(t_step, 90))},
-        "step_gbs_live_keys": live * KEY_BYTES_PER_POSITION / statistics.fmean(t_step) / 1e9,
+                       "step_p10": 1e6 * float(np.percentile(per_step, 10)),
+                       "step_p50": 1e6 * float(np.percentile(per_step, 50)),
+                       "step_p90": 1e6 * float(np.percentile(per_step, 90)),
+                       "percentiles": "per-step events" + ("" if args.l2_flush else
+                                                           " (separate loop, an event between steps)")},
+        "step_gbs_live_keys": live * KEY_BYTES_PER_POSITION / mean_step / 1e9,
+        "timing": ("events around every step, L2 flushed outside them" if args.l2_flush else
+                   "one CUDA-event pair around the K back-to-back steps"),
         "cpu_baseline": cpu,
         "context_scaling": scaling_1m,
         "fp8_key_cache": fp8,

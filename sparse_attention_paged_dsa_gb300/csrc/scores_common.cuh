@@ -14,8 +14,7 @@ namespace dsa {
 namespace scores {
 
 constexpr int kBatch = 32;         // units prepared per warp-wide page-table load
-constexpr int kChunk = 2;          // units per dynamic scheduling step
-constexpr int kStaticEighths = 7;  // share of the units assigned statically
+constexpr int kChunk = 1;          // units per dynamic scheduling step (the remainder)
 constexpr int kEndOfWork = -1;     // metadata marker: no more units
 static_assert(kChunk >= 1 && kChunk <= kBatch, "a chunk is prepared by one warp");
 
@@ -115,17 +114,19 @@ __device__ __forceinline__ UnitPrep prepare_units(const RowTable& t, const Score
     return c;
 }
 
-// The producer warp's unit schedule: first the CTA's equal contiguous share of
-// 7/8 of the units (in batches of kBatch), then kChunk-unit chunks of the last
-// eighth taken from a counter in the workspace header, each chunk number
-// requested one batch ahead.  All calls are warp-collective.
+// The producer warp's unit schedule: first the CTA's equal contiguous share
+// floor(U / grid) of the units (in batches of kBatch), then the fewer than
+// `grid` remaining units one at a time from a counter in the workspace header,
+// each number requested one batch ahead.  (Handing a larger share out
+// dynamically cost more in counter and page-table round trips than it won in
+// balance.)  All calls are warp-collective.
 struct UnitSchedule {
     int sp, se, dyn0, total, ticket;
     uint32_t* counter;
 
     __device__ __forceinline__ UnitSchedule(const ScoresParams& p, int total_units, int lane) {
         const int grid = gridDim.x;
-        const int S = static_cast<int>((int64_t(total_units) * kStaticEighths) / (8 * int64_t(grid)));
+        const int S = total_units / grid;
         sp = blockIdx.x * S;
         se = sp + S;
         dyn0 = grid * S;

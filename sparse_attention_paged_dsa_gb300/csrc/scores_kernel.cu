@@ -16,12 +16,11 @@
 //     device, so graph capture is safe and a 1M-token max_context launches the
 //     same grid as an 8K one.
 //   * Work unit = 2 consecutive pages of one request = 128 keys = 16 KiB.
-//     Each CTA first takes an equal contiguous range holding 7/8 of the
-//     batch's live units (few request changes per CTA); the last 1/8 is
-//     handed out in small chunks from a counter in the workspace header, so
-//     that CTAs that draw slower memory take fewer of them and all finish
-//     together.  The last CTA to leave resets the counter.  Cost is O(live
-//     units), not O(max_context).
+//     Each CTA takes an equal contiguous range of floor(U / grid) of the
+//     batch's U live units (few request changes per CTA); the fewer than
+//     `grid` units left over go one at a time to whichever CTAs ask first,
+//     from a counter in the workspace header.  The last CTA to leave resets
+//     the counter.  Cost is O(live units), not O(max_context).
 //   * Warp 0 (one lane issues) gathers pages with TMA tiled loads (128-byte
 //     swizzle) into a kStages ring of 16 KiB stages; page ids (and the next
 //     chunk number) are fetched one batch ahead.  The request's 4 KiB query
