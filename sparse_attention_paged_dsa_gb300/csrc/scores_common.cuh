@@ -14,13 +14,7 @@ namespace dsa {
 namespace scores {
 
 constexpr int kBatch = 32;         // units prepared per warp-wide page-table load
-constexpr int kChunk = 1;          // units per dynamic scheduling step (the remainder)
 constexpr int kEndOfWork = -1;     // metadata marker: no more units
-static_assert(kChunk >= 1 && kChunk <= kBatch, "a chunk is prepared by one warp");
-
-// Scheduling words in the 256-byte workspace header (word 0 is the error word).
-constexpr int kHeaderNextChunkWord = 32;  // byte 128
-constexpr int kHeaderExitWord = 48;       // byte 192
 
 // Unit metadata: request (10 bits), page pair within the request (15 bits),
 // validity of its two pages (2 bits).  Max row width 2^22 C4 positions keeps
@@ -114,40 +108,36 @@ __device__ __forceinline__ UnitPrep prepare_units(const RowTable& t, const Score
     return c;
 }
 
-// The producer warp's unit schedule: first the CTA's equal contiguous share
-// floor(U / grid) of the units (in batches of kBatch), then the fewer than
-// `grid` remaining units one at a time from a counter in the workspace header,
-// each number requested one batch ahead.  (Handing a larger share out
-// dynamically cost more in counter and page-table round trips than it won in
-// balance.)  All calls are warp-collective.
+// A CTA's units: the contiguous range [c S, (c + 1) S) with S = floor(U / grid),
+// in batches of kBatch, then unit S grid + c when c < U - S grid.  Fixed by
+// (U, grid, c) alone, so every producer warp of the CTA walks the same
+// sequence without talking to the others.  (A dynamic share handed out from
+// a global counter cost more in round trips than it won in balance.)
 struct UnitSchedule {
-    int sp, se, dyn0, total, ticket;
-    uint32_t* counter;
+    int sp, se, extra;
 
-    __device__ __forceinline__ UnitSchedule(const ScoresParams& p, int total_units, int lane) {
+    __device__ __forceinline__ explicit UnitSchedule(int total_units) {
         const int grid = gridDim.x;
         const int S = total_units / grid;
         sp = blockIdx.x * S;
         se = sp + S;
-        dyn0 = grid * S;
-        total = total_units;
-        counter = p.err + kHeaderNextChunkWord;
-        ticket = 0;
-        if (lane == 0) ticket = int(atomicAdd(counter, 1u));
+        extra = int(blockIdx.x) < total_units - S * grid ? S * grid + int(blockIdx.x) : -1;
     }
 
-    // Next batch [u0, u0 + cnt); cnt == 0 when the CTA has no more work.
-    __device__ __forceinline__ void next(int& u0, int& cnt, int lane) {
+    // Next batch [u0, u0 + cnt); cnt == 0 when the CTA has no more units.
+    __device__ __forceinline__ void next(int& u0, int& cnt) {
         if (sp < se) {
             u0 = sp;
             cnt = min(kBatch, se - sp);
             sp += cnt;
-            return;
+        } else if (extra >= 0) {
+            u0 = extra;
+            cnt = 1;
+            extra = -1;
+        } else {
+            u0 = 0;
+            cnt = 0;
         }
-        const int t = __shfl_sync(0xffffffffu, ticket, 0);
-        u0 = dyn0 + t * kChunk;
-        cnt = u0 < total ? min(kChunk, total - u0) : 0;
-        if (lane == 0 && cnt > 0) ticket = int(atomicAdd(counter, 1u));
     }
 };
 
@@ -164,16 +154,6 @@ __device__ __forceinline__ void fill_dead_tails(const RowTable& t, const ScoresP
         float4* row = reinterpret_cast<float4*>(p.out + int64_t(b) * M);
         for (int64_t i = extent / 4 + int64_t(blockIdx.x) * nthreads + et; i < M / 4; i += stride)
             __stcs(row + i, ninf4);
-    }
-}
-
-// Called by one thread per CTA after all its work: the last CTA out resets
-// the schedule words for the next launch (no CTA waits for another).
-__device__ __forceinline__ void release_schedule(const ScoresParams& p) {
-    __threadfence();
-    if (atomicAdd(p.err + kHeaderExitWord, 1u) == uint32_t(gridDim.x - 1)) {
-        atomicExch(p.err + kHeaderNextChunkWord, 0u);
-        atomicExch(p.err + kHeaderExitWord, 0u);
     }
 }
 

@@ -27,18 +27,19 @@
 // w_h * S_h * relu(acc[2h] + acc[2h+1] / 16), sums over heads and multiplies
 // by scale_t once.
 //
-// Pipeline (per CTA, two CTAs per SM, persistent grid sized by the device):
-//   * warp 0: the unit schedule and page ids (scores_common.cuh), staged per
-//     batch in shared memory; lane 0 then issues, per unit, two 4 KiB TMA
-//     code boxes (64-byte swizzle) into an 8-stage ring and posts the unit's
-//     page ids to the scale copier; per request change it stages the bf16
-//     query and its head weights (TMA) for the splitter.
-//   * warp 3: copies each unit's 2 x 256 B of scales into a scale ring with
-//     16-byte cp.async from its 32 lanes, which arrive on the stage's full
-//     barrier (a TMA instruction costs about as much issue time as a whole
-//     page, so the small scale rows do not go through TMA).
+// Pipeline (per CTA, three CTAs per SM, persistent grid sized by the device):
+//   * warps 0 and 3 (producers): the unit schedule and page ids
+//     (scores_common.cuh); warp 0 takes the CTA's even units, warp 3 the odd
+//     ones (one TMA-issuing thread keeps too few 4 KiB boxes in flight to
+//     cover HBM latency).  Per unit, lane 0 issues two TMA code boxes (64-byte
+//     swizzle) into the stage ring and all 32 lanes copy the 2 x 256 B of
+//     scales into a scale ring with 16-byte cp.async that arrive on the
+//     stage's full barrier (a TMA instruction costs about as much issue time
+//     as a whole page, so the small scale rows do not go through TMA).  Per
+//     request change the owner of the first unit stages the bf16 query and
+//     its head weights (TMA) for the splitter.
 //   * warp 2: per request change, splits the query into the hi/lo e4m3 tile
-//     the MMA reads (64-byte swizzle) and w_h * S_h, in a 4-slot ring that
+//     the MMA reads (64-byte swizzle) and w_h * S_h, in a small ring that
 //     the epilogue frees when it leaves the request.
 //   * warp 1: tcgen05.mma kind::f8f6f4, M=128 keys x N=64 x K=32, two per
 //     unit, into one of 4 TMEM accumulators of 64 columns.
@@ -62,9 +63,10 @@ namespace {
 
 using namespace scores;
 
-// Three CTAs per SM: one TMA-issuing thread keeps too few 4 KiB boxes in
-// flight to cover HBM latency, so the SM runs three independent pipelines.
-constexpr int kStages = 4;       // key-code stages of 8 KiB (two pages)
+// Three CTAs per SM, two TMA-issuing producer warps each: one issuing thread
+// keeps too few 4 KiB boxes in flight to cover HBM latency (a TMA instruction
+// takes about 120 cycles to issue), so each SM runs six issuers.
+constexpr int kStages = 4;       // key-code stages of 8 KiB (two pages), shared by the producer warps
 constexpr int kQRaw = 2;         // staged bf16 query rows
 constexpr int kQSlots = 2;       // split e4m3 query tiles
 constexpr int kAccStages = 2;
@@ -74,12 +76,12 @@ constexpr int kAccCols = 64;     // N = 2 x 32 heads
 constexpr uint32_t kTmemCols = kAccStages * kAccCols;  // 128
 constexpr int kConvThreads = 32;
 constexpr int kEpiThreads = 128;
-constexpr int kThreads = 128 + kEpiThreads;                // producer, MMA, splitter, scale copier, epilogue
+constexpr int kThreads = 128 + kEpiThreads;                // producers 0 and 3, MMA 1, splitter 2, epilogue 4..7
 constexpr int kStageBytes = 2 * kPageCodeBytes;            // 8 KiB: 128 keys x 64 B
 constexpr int kQ8Bytes = 2 * kHeads * kHeadDim;            // 4 KiB: 64 rows x 64 B
 constexpr int kUnitScaleBytes = 2 * kPageScaleBytes;       // 512 B
 constexpr int kWRowBytes = kHeads * 4;                     // 128 B
-constexpr uint32_t kFullArrivals = 1 + 32;                 // producer lane 0 + the copier's 32 lanes
+constexpr uint32_t kFullArrivals = 1 + 32;                 // producer lane 0 + its 32 lanes' scale copies
 constexpr uint32_t kIdesc = idesc_e4m3_f32(128, kAccCols);
 static_assert(kRing >= kStages + kAccStages + 1, "metadata ring too small");
 static_assert(kTmemCols * kCtasPerSm <= 512, "TMEM columns per SM");
@@ -95,12 +97,9 @@ struct __align__(16) SmemCtl {
     uint64_t tempty[kAccStages];
     uint64_t tmeta[kAccStages];
     uint64_t drain;
-    uint64_t unit_posted[kRing];  // a unit's metadata and page ids are readable (scale copier)
     uint32_t tmem_base;
     int abort;
     int32_t meta[kRing];
-    int2 unit_pages[kRing];       // valid page ids of each unit (-1: none)
-    int4 batch_units[kBatch];     // the producer's current batch: request, pair, page ids
     int32_t qrow[kQRaw];                      // request of each staged query (-1: no more)
     __align__(16) float wq[kQSlots][kHeads];  // w_h * S_h of each split query
     RowTable rows;
@@ -188,7 +187,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             mbar_init(&ctl.tmeta[a], 1);
         }
         mbar_init(&ctl.drain, 1);
-        for (int r = 0; r < kRing; ++r) mbar_init(&ctl.unit_posted[r], 1);
         ctl.abort = 0;
         fence_mbar_init();
         tma_prefetch_map(&codes_map);
@@ -201,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     pdl_wait_prior_grid();
     pdl_allow_next_grid();
-    if (warp == 2) build_row_table(ctl.rows, p, lane);
+    if (warp == 1) build_row_table(ctl.rows, p, lane);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -210,118 +208,128 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const uint32_t tmem_base = ctl.tmem_base;
     const int64_t M = p.row_width;
 
-    if (warp == 0) {
-        // ================= producer: schedule, page ids, TMA of codes, scales, queries =================
+    if (warp == 0 || warp == 3) {
+        // ================= producers: warp 0 issues the CTA's even units, warp 3 the odd ones =================
+        // Both walk the same unit sequence (page ids fetched one batch ahead).  Per own unit:
+        // lane 0 posts the metadata and issues the two code boxes; all 32 lanes copy the
+        // unit's scales (cp.async, arriving on the stage's full barrier).  A row change is
+        // numbered in sequence order; the warp owning the unit where the row starts stages
+        // the row's query and head weights for the splitter.
+        const int me = warp == 0 ? 0 : 1;
         const uint64_t pol_keys = l2_policy_evict_first();
         const uint64_t pol_q = l2_policy_evict_last();
-        int stage = 0, issued = 0, q_issued = 0, q_row = -1, seq = 0;
-        uint32_t phase = 0;
+        int seq = 0, nrows = 0, prev_b = -1, last_mine = -1;
+        int q_mine[kQRaw];  // the last row-change numbers whose query this warp staged
+#pragma unroll
+        for (int j = 0; j < kQRaw; ++j) q_mine[j] = -1;
         bool stop = false;
-        UnitSchedule sched(p, total_units, lane);
+
+        UnitSchedule sched(total_units);
         int cur_u0, cur_cnt;
-        sched.next(cur_u0, cur_cnt, lane);
+        sched.next(cur_u0, cur_cnt);
         UnitPrep cur = prepare_units(ctl.rows, p, cur_u0, cur_cnt, lane);
         while (cur_cnt > 0 && !stop) {
-            if (lane < cur_cnt) ctl.batch_units[lane] = make_int4(cur.b, cur.pair, cur.pg0, cur.pg1);
-            __syncwarp();
             int nxt_u0, nxt_cnt;
-            sched.next(nxt_u0, nxt_cnt, lane);
+            sched.next(nxt_u0, nxt_cnt);
             const UnitPrep nxt = prepare_units(ctl.rows, p, nxt_u0, nxt_cnt, lane);  // loads in flight
-            int failed = 0;
-            if (lane == 0) {
-                for (int i = 0; i < cur_cnt; ++i) {
-                    const int4 un = ctl.batch_units[i];
-                    const int bi = un.x, g0 = un.z, g1 = un.w;
-                    if (bi != q_row) {  // new request: stage its query and head weights for the splitter
-                        const int qs = q_issued % kQRaw;
-                        if (!mbar_wait(&ctl.qraw_empty[qs], ((q_issued / kQRaw) & 1) ^ 1u, &ctl.abort)) {
+            for (int i = 0; i < cur_cnt; ++i, ++seq) {
+                const int bi = __shfl_sync(0xffffffffu, cur.b, i);
+                const bool new_row = bi != prev_b;
+                if (new_row) {
+                    ++nrows;
+                    prev_b = bi;
+                }
+                if ((seq & 1) != me) continue;  // the other producer's unit
+                const int pi = __shfl_sync(0xffffffffu, cur.pair, i);
+                const int g0 = __shfl_sync(0xffffffffu, cur.pg0, i);
+                const int g1 = __shfl_sync(0xffffffffu, cur.pg1, i);
+                const bool ok0 = g0 >= 0 && g0 < p.num_pages;
+                const bool ok1 = g1 >= 0 && g1 < p.num_pages;
+                const int stage = seq % kStages;
+                int failed = 0;
+                if (lane == 0) {
+                    if (new_row) {  // stage the request's query and head weights for the splitter
+                        const int k = nrows - 1, qs = k % kQRaw;
+                        if (!mbar_wait(&ctl.qraw_empty[qs], ((k / kQRaw) & 1) ^ 1u, &ctl.abort)) {
                             failed = 1;
-                            break;
+                        } else {
+                            ctl.qrow[qs] = bi;
+                            mbar_arrive_expect_tx(&ctl.qraw_full[qs], kQRowBytes + kWRowBytes);
+                            tma_load_2d(qraw + size_t(qs) * kQRowBytes, &qraw_map, &ctl.qraw_full[qs], 0,
+                                        bi * kHeads, pol_q);
+                            tma_load_2d(tiles + kOffWRaw + size_t(qs) * kWRowBytes, &w_map, &ctl.qraw_full[qs], 0,
+                                        bi, pol_q);
+#pragma unroll
+                            for (int j = 0; j + 1 < kQRaw; ++j) q_mine[j] = q_mine[j + 1];
+                            q_mine[kQRaw - 1] = k;
                         }
-                        ctl.qrow[qs] = bi;
-                        mbar_arrive_expect_tx(&ctl.qraw_full[qs], kQRowBytes + kWRowBytes);
-                        tma_load_2d(qraw + size_t(qs) * kQRowBytes, &qraw_map, &ctl.qraw_full[qs], 0, bi * kHeads,
-                                    pol_q);
-                        tma_load_2d(tiles + kOffWRaw + size_t(qs) * kWRowBytes, &w_map, &ctl.qraw_full[qs], 0, bi,
-                                    pol_q);
-                        ++q_issued;
-                        q_row = bi;
                     }
-                    if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort)) {
+                    if (!failed && !mbar_wait(&ctl.empty[stage], (uint32_t(seq / kStages) & 1u) ^ 1u, &ctl.abort))
                         failed = 1;
-                        break;
-                    }
-                    const bool ok0 = g0 >= 0 && g0 < p.num_pages;
-                    const bool ok1 = g1 >= 0 && g1 < p.num_pages;
-                    if (!ok0 || (g1 != -2 && !ok1)) atomicOr(p.err, kErrBadPage);
-                    ctl.meta[seq % kRing] = pack_meta(bi, un.y, ok0, ok1);
-                    ctl.unit_pages[seq % kRing] = make_int2(ok0 ? g0 : -1, ok1 ? g1 : -1);
-                    mbar_arrive(&ctl.unit_posted[seq % kRing]);
-                    const uint32_t bytes = (ok0 ? kPageCodeBytes : 0) + (ok1 ? kPageCodeBytes : 0);
-                    uint8_t* a = tiles + size_t(stage) * kStageBytes;
-                    if (bytes != 0) {
-                        mbar_arrive_expect_tx(&ctl.full[stage], bytes);
-                        if (ok0) tma_load_3d(a, &codes_map, &ctl.full[stage], 0, 0, g0, pol_keys);
-                        if (ok1) tma_load_3d(a + kPageCodeBytes, &codes_map, &ctl.full[stage], 0, 0, g1, pol_keys);
-                    } else {
-                        mbar_arrive(&ctl.full[stage]);  // nothing to load
-                    }
-                    ++issued;
-                    ++seq;
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    if (!failed) {
+                        if (!ok0 || (g1 != -2 && !ok1)) atomicOr(p.err, kErrBadPage);
+                        ctl.meta[seq % kRing] = pack_meta(bi, pi, ok0, ok1);
+                        const uint32_t bytes = (ok0 ? kPageCodeBytes : 0) + (ok1 ? kPageCodeBytes : 0);
+                        uint8_t* a = tiles + size_t(stage) * kStageBytes;
+                        if (bytes != 0) {
+                            mbar_arrive_expect_tx(&ctl.full[stage], bytes);
+                            if (ok0) tma_load_3d(a, &codes_map, &ctl.full[stage], 0, 0, g0, pol_keys);
+                            if (ok1) tma_load_3d(a + kPageCodeBytes, &codes_map, &ctl.full[stage], 0, 0, g1, pol_keys);
+                        } else {
+                            mbar_arrive(&ctl.full[stage]);  // nothing to load
+                        }
+                        last_mine = seq;
                     }
                 }
+                if (__shfl_sync(0xffffffffu, failed, 0)) {
+                    stop = true;
+                    break;
+                }
+                {  // lane l copies 16 B of scales: page l / 16, entries 4 (l % 16) .. + 3
+                    const int g = lane < 16 ? g0 : g1;
+                    const bool ok = lane < 16 ? ok0 : ok1;
+                    if (ok)
+                        cp_async_16(tiles + kOffScales + size_t(seq % kRing) * kUnitScaleBytes + lane * 16,
+                                    p.key_scales + int64_t(g) * kPageEntries + (lane & 15) * 4);
+                    cp_async_arrive_noinc(&ctl.full[stage]);
+                }
             }
-            __syncwarp();
-            stop = __shfl_sync(0xffffffffu, failed, 0) != 0;
-            seq = __shfl_sync(0xffffffffu, seq, 0);
-            stage = __shfl_sync(0xffffffffu, stage, 0);
-            phase = __shfl_sync(0xffffffffu, phase, 0);
-            issued = __shfl_sync(0xffffffffu, issued, 0);
-            q_issued = __shfl_sync(0xffffffffu, q_issued, 0);
-            q_row = __shfl_sync(0xffffffffu, q_row, 0);
             cur_u0 = nxt_u0;
             cur_cnt = nxt_cnt;
             cur = nxt;
         }
-        if (!stop) {  // end-of-work markers: one for the splitters, one for the MMA issuer and epilogue
+        // End-of-work markers, posted by the warp that owns the end place: one for the splitter
+        // (row-change number nrows), one for the MMA issuer and epilogue (unit number seq).
+        if (!stop && (seq & 1) == me) {
+            const int stage = seq % kStages;
             int failed = 0;
             if (lane == 0) {
-                const int qs = q_issued % kQRaw;
-                if (!mbar_wait(&ctl.qraw_empty[qs], ((q_issued / kQRaw) & 1) ^ 1u, &ctl.abort) ||
-                    !mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort)) {
+                const int qs = nrows % kQRaw;
+                if (!mbar_wait(&ctl.qraw_empty[qs], ((nrows / kQRaw) & 1) ^ 1u, &ctl.abort) ||
+                    !mbar_wait(&ctl.empty[stage], (uint32_t(seq / kStages) & 1u) ^ 1u, &ctl.abort)) {
                     failed = 1;
                 } else {
                     ctl.qrow[qs] = -1;
                     mbar_arrive(&ctl.qraw_full[qs]);
                     ctl.meta[seq % kRing] = kEndOfWork;
-                    mbar_arrive(&ctl.unit_posted[seq % kRing]);
                     mbar_arrive(&ctl.full[stage]);
                 }
             }
             if (__shfl_sync(0xffffffffu, failed, 0)) stop = true;
+            else cp_async_arrive_noinc(&ctl.full[stage]);
         }
         if (lane == 0 && stop) {
             atomicOr(p.err, kErrWaitTimeout);
             ctl.abort = 1;
         }
-        if (lane == 0 && ctl.abort) {  // let every copy this CTA issued land before it may exit
-            int s = stage;
-            uint32_t ph = phase;
-            for (int i = 0; i < min(issued, kStages); ++i) {
-                if (s == 0) {
-                    s = kStages - 1;
-                    ph ^= 1u;
-                } else {
-                    --s;
-                }
-                wait_landed(&ctl.full[s], ph);
-            }
-            for (int j = max(0, q_issued - kQRaw); j < q_issued; ++j)
-                wait_landed(&ctl.qraw_full[j % kQRaw], (j / kQRaw) & 1);
+        if (lane == 0 && ctl.abort) {  // let every copy this warp issued land before the CTA may exit
+            for (int s2 = last_mine; s2 >= 0 && s2 > last_mine - kStages; s2 -= 2)  // this warp's stages
+                wait_landed(&ctl.full[s2 % kStages], uint32_t(s2 / kStages) & 1u);
+#pragma unroll
+            for (int j = 0; j < kQRaw; ++j)
+                if (q_mine[j] >= 0) wait_landed(&ctl.qraw_full[q_mine[j] % kQRaw], uint32_t(q_mine[j] / kQRaw) & 1u);
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");  // no scale copy outlives the CTA
     } else if (warp == 1) {
         // ================= MMA issuer (one lane) =================
         if (lane == 0) {
@@ -438,32 +446,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             atomicOr(p.err, kErrWaitTimeout);
             ctl.abort = 1;
         }
-    } else if (warp == 3) {
-        // ================= scale copier: 2 x 256 B of key scales per unit =================
-        bool stop = false;
-        for (int seq = 0;; ++seq) {
-            const int r = seq % kRing;
-            if (!mbar_wait(&ctl.unit_posted[r], (seq / kRing) & 1, &ctl.abort)) {
-                stop = true;
-                break;
-            }
-            const bool end = ctl.meta[r] == kEndOfWork;
-            if (!end) {  // lane l: page l / 16, entries 4 (l % 16) .. + 3
-                const int2 pg = ctl.unit_pages[r];
-                const int g = lane < 16 ? pg.x : pg.y;
-                if (g >= 0)
-                    cp_async_16(tiles + kOffScales + size_t(r) * kUnitScaleBytes + lane * 16,
-                                p.key_scales + int64_t(g) * kPageEntries + (lane & 15) * 4);
-            }
-            cp_async_arrive_noinc(&ctl.full[seq % kStages]);
-            if (end) break;
-        }
-        if (stop && lane == 0) {
-            atomicOr(p.err, kErrWaitTimeout);
-            ctl.abort = 1;
-        }
-        asm volatile("cp.async.wait_all;" ::: "memory");  // no scale copy outlives the CTA
-    } else {
+    } else if (warp >= 4) {
         // ================= epilogue: warps 4..7 =================
         const int et = threadIdx.x - 128;  // 0..127
         const int quad = warp & 3;         // TMEM lanes [32*quad, 32*quad + 32)
@@ -538,7 +521,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     tc_fence_before_sync();
     __syncthreads();
-    if (threadIdx.x == 0) release_schedule(p);
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, kTmemCols);

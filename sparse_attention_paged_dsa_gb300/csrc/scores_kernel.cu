@@ -21,12 +21,14 @@
 //     `grid` units left over go one at a time to whichever CTAs ask first,
 //     from a counter in the workspace header.  The last CTA to leave resets
 //     the counter.  Cost is O(live units), not O(max_context).
-//   * Warp 0 (one lane issues) gathers pages with TMA tiled loads (128-byte
-//     swizzle) into a kStages ring of 16 KiB stages; page ids (and the next
-//     chunk number) are fetched one batch ahead.  The request's 4 KiB query
-//     tile is loaded once per request change into a small ring of its own.
-//     Each unit's request, page pair and page validity go to a small
-//     metadata ring.
+//   * Two producer warps (one lane each issues) gather pages with TMA tiled
+//     loads (128-byte swizzle) into a kStages ring of 16 KiB stages: warp 0
+//     the CTA's even units, warp 2 the odd ones.  One issuing thread keeps
+//     too few page boxes in flight to cover HBM latency; two per CTA do.
+//     Page ids are fetched one batch ahead.  The request's 4 KiB query tile
+//     is loaded once per request change into a small ring of its own.  Each
+//     unit's request, page pair and page validity go to a small metadata
+//     ring.
 //   * Warp 1 (one lane) issues tcgen05.mma kind::f16, M=128 keys x N=32 heads
 //     x K=64 dims (4 instructions of K=16) into one of 4 TMEM accumulators of
 //     32 fp32 columns, then publishes the accumulator and the unit's metadata.
@@ -56,18 +58,19 @@ namespace {
 
 using namespace scores;
 
-// Three CTAs per SM: one TMA-issuing thread keeps too few page boxes in
-// flight to cover HBM latency, so the SM runs three independent pipelines.
-constexpr int kStages = 3;                             // 16 KiB stages per CTA
+// Three CTAs per SM, two TMA-issuing producer warps each: one issuing thread
+// keeps too few page boxes in flight to cover HBM latency (a TMA instruction
+// takes about 120 cycles to issue), so each SM runs six issuers.
+constexpr int kStages = 3;                             // 16 KiB stages per CTA, shared by the producer warps
 constexpr int kEpiGroups = 1;                          // epilogue groups of 4 warps
-constexpr int kCtasPerSm = 3;                          // three independent pipelines per SM
+constexpr int kCtasPerSm = 3;
 constexpr int kQSlots = 2;
 constexpr int kAccStages = 4;
 constexpr int kMetaRing = 16;                          // >= kStages + kAccStages + 1
 constexpr int kAccCols = 32;                           // fp32 columns per accumulator (N = 32 heads)
 constexpr uint32_t kTmemCols = kAccStages * kAccCols;  // 128 (power of two >= 32)
 constexpr int kEpiThreads = 128 * kEpiGroups;
-constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kThreads = 128 + kEpiThreads;           // producers 0 and 2, MMA 1, set-up 3, epilogue 4..
 constexpr int kStageBytes = 2 * kPageBytes;            // 16 KiB: 128 keys x 128 B
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kAccCols);
 static_assert(kAccStages % kEpiGroups == 0, "each epilogue group owns whole accumulator stages");
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     pdl_allow_next_grid();
 
     // ---- per-row live counts and unit prefix.
-    if (warp == 2) build_row_table(ctl.rows, p, lane);
+    if (warp == 3) build_row_table(ctl.rows, p, lane);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -143,42 +146,56 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const uint32_t tmem_base = ctl.tmem_base;
     const int64_t M = p.row_width;
 
-    if (warp == 0) {
-        // ================= producer: schedule, page ids, TMA gathers =================
+    if (warp == 0 || warp == 2) {
+        // ================= producers: warp 0 issues the CTA's even units, warp 2 the odd ones =================
+        // Both walk the same unit sequence (page ids fetched one batch ahead); a row change is
+        // numbered in sequence order and its query tile is loaded by the warp that owns the
+        // unit where the row starts.
+        const int me = warp >> 1;
         const uint64_t pol_keys = l2_policy_evict_first();
         const uint64_t pol_q = l2_policy_evict_last();
-        int stage = 0;
-        uint32_t phase = 0;
-        int issued = 0, q_issued = 0, q_row = -1, seq = 0;
+        int seq = 0, nrows = 0, prev_b = -1, last_mine = -1;
+        int q_mine[kQSlots];  // the last row-change numbers whose query this warp loaded
+#pragma unroll
+        for (int j = 0; j < kQSlots; ++j) q_mine[j] = -1;
         bool stop = false;
 
-        UnitSchedule sched(p, total_units, lane);
+        UnitSchedule sched(total_units);
         int cur_u0, cur_cnt;
-        sched.next(cur_u0, cur_cnt, lane);
+        sched.next(cur_u0, cur_cnt);
         UnitPrep cur = prepare_units(ctl.rows, p, cur_u0, cur_cnt, lane);
         while (cur_cnt > 0 && !stop) {
             int nxt_u0, nxt_cnt;
-            sched.next(nxt_u0, nxt_cnt, lane);
+            sched.next(nxt_u0, nxt_cnt);
             const UnitPrep nxt = prepare_units(ctl.rows, p, nxt_u0, nxt_cnt, lane);  // loads in flight
-            for (int i = 0; i < cur_cnt; ++i) {
+            for (int i = 0; i < cur_cnt; ++i, ++seq) {
                 const int bi = __shfl_sync(0xffffffffu, cur.b, i);
+                const bool new_row = bi != prev_b;
+                if (new_row) {
+                    ++nrows;
+                    prev_b = bi;
+                }
+                if ((seq & 1) != me) continue;  // the other producer's unit
                 const int pi = __shfl_sync(0xffffffffu, cur.pair, i);
                 const int g0 = __shfl_sync(0xffffffffu, cur.pg0, i);
                 const int g1 = __shfl_sync(0xffffffffu, cur.pg1, i);
                 int failed = 0;
                 if (lane == 0) {
-                    if (bi != q_row) {  // new request: its query tile goes to the next q slot
-                        const int qs = q_issued % kQSlots;
-                        if (!mbar_wait(&ctl.qempty[qs], ((q_issued / kQSlots) & 1) ^ 1u, &ctl.abort)) {
+                    if (new_row) {  // this request's query tile goes to the row's q slot
+                        const int k = nrows - 1, qs = k % kQSlots;
+                        if (!mbar_wait(&ctl.qempty[qs], ((k / kQSlots) & 1) ^ 1u, &ctl.abort)) {
                             failed = 1;
                         } else {
                             mbar_arrive_expect_tx(&ctl.qfull[qs], kQRowBytes);
                             tma_load_2d(qtiles + size_t(qs) * kQRowBytes, &q_map, &ctl.qfull[qs], 0, bi * kHeads,
                                         pol_q);
-                            ++q_issued;
-                            q_row = bi;
+#pragma unroll
+                            for (int j = 0; j + 1 < kQSlots; ++j) q_mine[j] = q_mine[j + 1];
+                            q_mine[kQSlots - 1] = k;
                         }
                     }
+                    const int stage = seq % kStages;
+                    const uint32_t phase = uint32_t(seq / kStages) & 1u;
                     if (!failed && !mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort)) failed = 1;
                     if (!failed) {
                         const bool ok0 = g0 >= 0 && g0 < p.num_pages;
@@ -194,60 +211,45 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         } else {
                             mbar_arrive(&ctl.full[stage]);  // nothing to load: the stage is full at once
                         }
-                        ++issued;
+                        last_mine = seq;
                     }
                 }
                 if (__shfl_sync(0xffffffffu, failed, 0)) {
                     stop = true;
                     break;
                 }
-                ++seq;
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
             }
             cur_u0 = nxt_u0;
             cur_cnt = nxt_cnt;
             cur = nxt;
         }
-        // One end-of-work marker per epilogue group.
-        for (int g = 0; g < kEpiGroups && !stop; ++g) {
+        // One end-of-work marker per epilogue group, each posted by the warp that owns its place.
+        for (int e = 0; e < kEpiGroups && !stop; ++e) {
+            const int s_end = seq + e;
+            if ((s_end & 1) != me) continue;
             int failed = 0;
             if (lane == 0) {
-                if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort)) {
+                const int stage = s_end % kStages;
+                if (!mbar_wait(&ctl.empty[stage], (uint32_t(s_end / kStages) & 1u) ^ 1u, &ctl.abort)) {
                     failed = 1;
                 } else {
-                    ctl.meta[seq % kMetaRing] = kEndOfWork;
+                    ctl.meta[s_end % kMetaRing] = kEndOfWork;
                     mbar_arrive(&ctl.full[stage]);
                 }
             }
             if (__shfl_sync(0xffffffffu, failed, 0)) stop = true;
-            ++seq;
-            if (++stage == kStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
         }
         if (lane == 0 && stop) {
             atomicOr(p.err, kErrWaitTimeout);
             ctl.abort = 1;
         }
-        // Let every copy this CTA issued land before the CTA may exit.
+        // Let every copy this warp issued land before the CTA may exit.
         if (lane == 0 && ctl.abort) {
-            int s = stage;
-            uint32_t ph = phase;
-            for (int i = 0; i < min(issued, kStages); ++i) {
-                if (s == 0) {
-                    s = kStages - 1;
-                    ph ^= 1u;
-                } else {
-                    --s;
-                }
-                wait_landed(&ctl.full[s], ph);
-            }
-            for (int j = max(0, q_issued - kQSlots); j < q_issued; ++j)
-                wait_landed(&ctl.qfull[j % kQSlots], (j / kQSlots) & 1);
+            for (int s2 = last_mine; s2 >= 0 && s2 > last_mine - kStages; s2 -= 2)  // this warp's stages
+                wait_landed(&ctl.full[s2 % kStages], uint32_t(s2 / kStages) & 1u);
+#pragma unroll
+            for (int j = 0; j < kQSlots; ++j)
+                if (q_mine[j] >= 0) wait_landed(&ctl.qfull[q_mine[j] % kQSlots], uint32_t(q_mine[j] / kQSlots) & 1u);
         }
     } else if (warp == 1) {
         // ================= MMA issuer (one lane) =================
@@ -307,10 +309,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             wait_landed(&ctl.drain, 0);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 4) {
         // ================= epilogue: kEpiGroups groups of 4 warps =================
-        const int et = threadIdx.x - 64;    // 0 .. kEpiThreads-1
-        const int group = (warp - 2) >> 2;  // takes the group-th, (group + kEpiGroups)-th, ... units
+        const int et = threadIdx.x - 128;   // 0 .. kEpiThreads-1
+        const int group = (warp - 4) >> 2;  // takes the group-th, (group + kEpiGroups)-th, ... units
         const int quad = warp & 3;          // TMEM lanes [32*quad, 32*quad + 32)
         const float neg_inf = __int_as_float(0xff800000);
 
@@ -378,7 +380,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     tc_fence_before_sync();
     __syncthreads();
-    if (threadIdx.x == 0) release_schedule(p);
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, kTmemCols);

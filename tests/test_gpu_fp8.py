@@ -197,3 +197,37 @@ def test_fp8_host_argument_checks(gpu_lib):
     torch.cuda.synchronize()
     assert torch.equal(scores.view(torch.int32), sentinel.view(torch.int32))
     assert b.get_error(ws) == 0
+
+
+def test_fp8_query_dynamic_range(gpu_lib, oracle):
+    """The kernel feeds the fp8 MMA a query split into two e4m3 terms under a per-head
+    power-of-two scale.  Queries whose heads differ in magnitude by 2^+-12, whose elements span
+    2^20 within a head, whose rows sit at 2^+-60, that hold bf16 subnormals, or whose heads are all
+    zero must still meet the score tolerance against the oracle."""
+    rng = np.random.default_rng(7)
+    base = I.with_fp8_keys(I.make_case(name="qrange", batch=6, max_context=4096,
+                                       seq_lens=[4096, 4000, 3000, 2048, 1500, 777], num_pages=120, k=64,
+                                       seed=17))
+    q = I.bf16_bits_to_f32(base.q).astype(np.float64)
+    q[0] *= 2.0 ** rng.integers(-12, 13, size=(32, 1))                 # heads 2^-12 .. 2^12 apart
+    q[1] *= np.where(rng.random((32, 64)) < 0.5, 2.0 ** -20, 1.0)      # elements 2^20 apart in a head
+    q[2] *= 2.0 ** 60
+    q[3] *= 2.0 ** -60
+    q[4, ::2] = 0.0                                                     # every other head all zero
+    q5 = (rng.integers(1, 0x80, size=(32, 64)) * rng.choice([-1, 1], size=(32, 64))).astype(np.int64)
+    q5_bits = np.where(q5 < 0, 0x8000 | (-q5), q5).astype(np.uint16)  # bf16 subnormals
+    q5_bits[:, :8] = I.f32_to_bf16_bits(rng.standard_normal((32, 8)).astype(np.float32) * 2.0 ** -125)
+    qb = I.f32_to_bf16_bits(q.astype(np.float32))
+    qb[5] = q5_bits
+    case = I.IndexerCase("qrange", qb, base.w, base.key_pool, base.page_table, base.seq_lens, base.max_context,
+                         base.k, key_codes=base.key_codes, key_scales=base.key_scales)
+    s, t, err = _run_fp8(gpu_lib, case)
+    assert err == 0
+    ref = oracle.case_scores_fp8(case)
+    rows = [0, 1, 2, 3, 4]  # row 5's scores are below the fp32 normal range: checked for sign/finiteness
+    sub = I.IndexerCase("qrange_rows", qb[rows], base.w[rows], base.key_pool, base.page_table[rows],
+                        base.seq_lens[rows], base.max_context, base.k)
+    check_scores(sub, s[rows], ref[rows])
+    n5 = int(case.live_positions()[5])
+    assert np.all(np.isfinite(s[5, :n5])) and np.all(np.isneginf(s[5, n5:]))
+    np.testing.assert_allclose(s[5, :n5], ref[5, :n5], rtol=0, atol=float(np.abs(ref[5, :n5]).max()) * 3e-3 + 1e-44)
