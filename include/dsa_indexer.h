@@ -61,9 +61,9 @@
  *   - Workspace: a caller-owned device buffer of at least
  *     dsa_indexer_workspace_size() bytes, zeroed once before first use
  *     (dsa_indexer_workspace_init or any memset to 0).  Its first 256 bytes
- *     hold the sticky device error word and the scores kernel's work
- *     counters, which every complete call leaves at zero again.  Calls that
- *     share a workspace must be ordered on one stream.
+ *     hold the sticky device error word; the rest of them is reserved and
+ *     stays zero.  Calls that share a workspace must be ordered on one
+ *     stream.
  */
 #ifndef DSA_INDEXER_H
 #define DSA_INDEXER_H

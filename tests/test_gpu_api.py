@@ -157,6 +157,6 @@ def test_cuda_graph_replay_with_new_contents(gpu_lib, oracle, with_row):
             np.testing.assert_array_equal(scores.cpu().numpy().view(np.uint32),
                                           s_ref.cpu().numpy().view(np.uint32))
     assert b.get_error(ws) == 0
-    # the work counters in the header are back at zero after every complete call
+    # the reserved header words stay zero
     torch.cuda.synchronize()
     assert int(ws[:256].view(torch.int32)[1:].abs().sum()) == 0
