@@ -62,6 +62,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context-scaling", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the fp8 key-cache measurement")
+    ap.add_argument("--no-mtp", action="store_true", help="skip the multi-token (next_n = 2, 4) measurement")
     ap.add_argument("--l2-flush", action="store_true",
                     help="memset a 512 MiB buffer before every timed launch (default: back-to-back steps; "
                          "the live keys are twice the L2)")
@@ -332,6 +333,48 @@ def run_fp8(args, case, binding, inputs, device, stream, live):
             "step": "dsa_indexer_fused_fp8 with the full-width scores row"}
 
 
+def run_mtp(args, case, binding, inputs, device, stream, live, pool, table, seq):
+    """The same workload with next_n query tokens per request (keys read once for all tokens)."""
+    import torch
+    out = {}
+    peak, peak_kind = measured_hbm_peak()
+    for Q in (2, 4):
+        c = inputs.with_next_n(case, Q)
+        q = torch.from_numpy(c.q.view("int16")).to(device).view(torch.bfloat16)
+        w = torch.from_numpy(c.w).to(device)
+        B, M, K = c.batch, c.max_context // 4, c.k
+        scores = torch.empty((B, Q, M), dtype=torch.float32, device=device)
+        topk = torch.empty((B, Q, K), dtype=torch.int32, device=device)
+        ws = torch.zeros(256, dtype=torch.uint8, device=device)
+
+        def step():
+            binding.dsa_indexer_fused_mtp(q, w, pool, table, seq, c.max_context, K, topk_idx=topk, scores=scores,
+                                          workspace=ws)
+
+        def scores_only():
+            binding.dsa_indexer_scores_mtp(q, w, pool, table, seq, c.max_context, scores=scores, workspace=ws)
+
+        for _ in range(max(3, args.warmup)):
+            step()
+            scores_only()
+        torch.cuda.synchronize(device)
+        n = max(10, min(args.steps, 300))
+        t_step, _ = time_loop(step, n, stream)
+        t_scores, _ = time_loop(scores_only, n, stream)
+        if binding.get_error(ws) != 0:
+            raise RuntimeError("device error word set in the multi-token run")
+        tok_positions = sum((max(int(L) - (Q - 1 - j), 0) + 3) // 4 for L in c.seq_lens for j in range(Q))
+        achieved = live * KEY_BYTES_PER_POSITION / t_scores / 1e9
+        out[str(Q)] = {"value": tok_positions / t_step, "unit": "token-positions/s", "ms_per_step": 1e3 * t_step,
+                       "scores_kernel_us": 1e6 * t_scores,
+                       "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                                    "frac": achieved / peak, "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
+                                    "algorithmic_bytes_per_launch": live * KEY_BYTES_PER_POSITION}}
+    out["step"] = ("dsa_indexer_fused_mtp with full-width rows: next_n query tokens per request, token j "
+                   "scores its causal prefix of seq_len - (next_n - 1 - j) tokens; keys read once")
+    return out
+
+
 def workload_config(case, world, l2_flush=False):
     live = int(case.live_positions().sum())
     return {"workload": case.name, "batch": case.batch, "max_context": case.max_context,
@@ -460,6 +503,8 @@ def run_ours(args):
 
     scaling_1m = context_scaling(binding, inputs, device) if not args.no_context_scaling else None
     fp8 = run_fp8(args, case, binding, inputs, device, stream, live) if not args.no_fp8 else None
+    mtp = (run_mtp(args, case, binding, inputs, device, stream, live, pool, table, seq)
+           if not args.no_mtp else None)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -495,6 +540,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "context_scaling": scaling_1m,
         "fp8_key_cache": fp8,
+        "multi_token": mtp,
         "e2e": e2e,
         "gpu_launches": 2 * n * world,
         "step": "dsa_indexer_fused with the full-width scores row (scores kernel, then top-k kernel)",

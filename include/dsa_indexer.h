@@ -199,6 +199,47 @@ DSA_API dsa_status_t dsa_indexer_fused_fp8(const void *q, const float *w, const 
                                    size_t workspace_bytes, void *stream);
 
 /*
+ * Multi-token decoding (the MTP / EAGLE draft tokens the deployment tried to
+ * enable: "The Indexer O(max_context) Breakthrough", section "MTP/EAGLE
+ * Integration (Phase 2)"): next_n query tokens per request score the same
+ * paged keys.  The pages give
+ * no per-token rule; reading used here: the request's seq_len counts all
+ * next_n tokens, and token j (0-based) sees its causal prefix of
+ * L_j = seq_len - (next_n - 1 - j) tokens, i.e. n_bj = ceil(max(L_j, 0) / 4)
+ * keys.  Token j of request b is row b x next_n + j of every output.
+ * Layouts (C-contiguous): q bf16 [batch, next_n, 32, 64], w fp32
+ * [batch, next_n, 32], scores fp32 [batch, next_n, max_context / 4],
+ * topk_idx int32 [batch, next_n, k]; key_pool, page_table, seq_lens as above.
+ * The keys are read once for all next_n tokens.  1 <= next_n <= 4.  next_n = 1
+ * gives exactly the results of the single-token entry points.
+ */
+#define DSA_MAX_NEXT_N 4
+
+/* Workspace bytes for the multi-token entry points (0 for an invalid shape). */
+DSA_API size_t dsa_indexer_workspace_size_mtp(int32_t batch, int32_t next_n, int64_t max_context, int32_t k);
+
+/* dsa_indexer_scores for next_n tokens per request. */
+DSA_API dsa_status_t dsa_indexer_scores_mtp(const void *q, const float *w, const void *key_pool,
+                                    int64_t num_pages, const int32_t *page_table,
+                                    const int32_t *seq_lens, int32_t batch, int32_t next_n,
+                                    int64_t max_context, float *scores, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/* dsa_indexer_topk over the batch x next_n rows, each with its own causal length. */
+DSA_API dsa_status_t dsa_indexer_topk_mtp(const float *scores, const int32_t *seq_lens, int32_t batch,
+                                  int32_t next_n, int64_t max_context, int32_t k,
+                                  int32_t *topk_idx, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/* dsa_indexer_fused for next_n tokens per request (same rules for scores_opt and workspace). */
+DSA_API dsa_status_t dsa_indexer_fused_mtp(const void *q, const float *w, const void *key_pool,
+                                   int64_t num_pages, const int32_t *page_table,
+                                   const int32_t *seq_lens, int32_t batch, int32_t next_n,
+                                   int64_t max_context, int32_t k, int32_t *topk_idx,
+                                   float *scores_opt, void *workspace, size_t workspace_bytes,
+                                   void *stream);
+
+/*
  * Read the sticky device error word into *code (host pointer).  Synchronises
  * `stream` (not capture-safe).  clear != 0 zeroes the word afterwards.
  */

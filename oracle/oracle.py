@@ -176,6 +176,39 @@ def case_scores_fp8(case) -> np.ndarray:
                       case.max_context)
 
 
+def scores_mtp(q, w, key_pool, page_table, seq_lens, max_context: int) -> np.ndarray:
+    """fp64 scores [B, Q, max_context/4] for Q query tokens per request (q [B, Q, H, D], w [B, Q, H]).
+
+    Token j is an ordinary indexer query whose sequence is the request's first
+    seq_len - (Q - 1 - j) tokens (its causal prefix; the request's seq_len counts
+    all Q tokens): the single-token definition applied once per token."""
+    q = np.asarray(q)
+    w = np.asarray(w)
+    B, Q = q.shape[0], q.shape[1]
+    seq = np.asarray(seq_lens, dtype=np.int64)
+    out = np.empty((B, Q, max_context // 4), dtype=np.float64)
+    for j in range(Q):
+        seq_j = np.maximum(seq - (Q - 1 - j), 0).astype(np.int32)
+        out[:, j] = scores(q[:, j], w[:, j], key_pool, page_table, seq_j, max_context)
+    return out
+
+
+def topk_mtp(rows, seq_lens, max_context: int, k: int) -> np.ndarray:
+    """Top-k [B, Q, k] of score rows [B, Q, max_context/4], token j with its own causal length."""
+    rows = np.asarray(rows)
+    B, Q = rows.shape[0], rows.shape[1]
+    seq = np.asarray(seq_lens, dtype=np.int64)
+    out = np.empty((B, Q, k), dtype=np.int32)
+    for j in range(Q):
+        seq_j = np.maximum(seq - (Q - 1 - j), 0).astype(np.int32)
+        out[:, j] = topk(rows[:, j], seq_j, max_context, k)
+    return out
+
+
+def case_scores_mtp(case) -> np.ndarray:
+    return scores_mtp(case.q, case.w, case.key_pool, case.page_table, case.seq_lens, case.max_context)
+
+
 def case_scores(case) -> np.ndarray:
     return scores(case.q, case.w, case.key_pool, case.page_table, case.seq_lens, case.max_context)
 

@@ -60,6 +60,14 @@ def load():
     lib.dsa_indexer_scores_fp8.restype = st
     lib.dsa_indexer_fused_fp8.argtypes = [p, p, p, p, i64, p, p, i32, i64, i32, p, p, p, sz, p]
     lib.dsa_indexer_fused_fp8.restype = st
+    lib.dsa_indexer_workspace_size_mtp.argtypes = [i32, i32, i64, i32]
+    lib.dsa_indexer_workspace_size_mtp.restype = sz
+    lib.dsa_indexer_scores_mtp.argtypes = [p, p, p, i64, p, p, i32, i32, i64, p, p, sz, p]
+    lib.dsa_indexer_scores_mtp.restype = st
+    lib.dsa_indexer_topk_mtp.argtypes = [p, p, i32, i32, i64, i32, p, p, sz, p]
+    lib.dsa_indexer_topk_mtp.restype = st
+    lib.dsa_indexer_fused_mtp.argtypes = [p, p, p, i64, p, p, i32, i32, i64, i32, p, p, p, sz, p]
+    lib.dsa_indexer_fused_mtp.restype = st
     lib.dsa_indexer_get_error.argtypes = [p, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, p]
     lib.dsa_indexer_get_error.restype = st
     lib.dsa_status_string.argtypes = [st]
@@ -224,6 +232,81 @@ def dsa_indexer_fused_fp8(q, w, key_codes, key_scales, page_table, seq_lens, max
                                       _ptr(scores), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(q.device))
     _check(st, "dsa_indexer_fused_fp8")
+    return topk_idx
+
+
+def _mtp_args(q, w, key_pool, page_table, seq_lens, max_context):
+    if q.dim() != 4:
+        raise ValueError(f"q must be [batch, next_n, 32, 64], got {tuple(q.shape)}")
+    B, Q = q.shape[0], q.shape[1]
+    _need(q, "q", _BF16, (B, Q, HEADS, HEAD_DIM))
+    _need(w, "w", (torch.float32,), (B, Q, HEADS))
+    _need(key_pool, "key_pool", _BF16)
+    if key_pool.dim() != 3 or tuple(key_pool.shape[1:]) != (PAGE_ENTRIES, HEAD_DIM):
+        raise ValueError(f"key_pool must be [num_pages, 64, 64], got {tuple(key_pool.shape)}")
+    _need(page_table, "page_table", (torch.int32,), (B, max_context // PAGE_TOKENS))
+    _need(seq_lens, "seq_lens", (torch.int32,), (B,))
+    return B, Q
+
+
+def workspace_size_mtp(batch: int, next_n: int, max_context: int, k: int = 1) -> int:
+    return int(load().dsa_indexer_workspace_size_mtp(batch, next_n, max_context, k))
+
+
+def dsa_indexer_scores_mtp(q, w, key_pool, page_table, seq_lens, max_context: int, scores=None, workspace=None):
+    """Scores [B, next_n, max_context/4] for next_n query tokens per request (q [B, next_n, 32, 64])."""
+    B, Q = _mtp_args(q, w, key_pool, page_table, seq_lens, max_context)
+    M = max_context // 4
+    if scores is None:
+        scores = torch.empty((B, Q, M), dtype=torch.float32, device=q.device)
+    _need(scores, "scores", (torch.float32,), (B, Q, M))
+    if workspace is None:
+        workspace = torch.zeros(WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=q.device)
+    st = load().dsa_indexer_scores_mtp(_ptr(q), _ptr(w), _ptr(key_pool), key_pool.shape[0], _ptr(page_table),
+                                       _ptr(seq_lens), B, Q, max_context, _ptr(scores), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(q.device))
+    _check(st, "dsa_indexer_scores_mtp")
+    return scores
+
+
+def dsa_indexer_topk_mtp(scores, seq_lens, max_context: int, k: int, topk_idx=None, workspace=None):
+    """Top-k [B, next_n, k] of each token's row (token j sees seq_len - (next_n - 1 - j) tokens)."""
+    if scores.dim() != 3:
+        raise ValueError(f"scores must be [batch, next_n, max_context/4], got {tuple(scores.shape)}")
+    B, Q = scores.shape[0], scores.shape[1]
+    _need(scores, "scores", (torch.float32,), (B, Q, max_context // 4))
+    _need(seq_lens, "seq_lens", (torch.int32,), (B,))
+    if topk_idx is None:
+        topk_idx = torch.empty((B, Q, k), dtype=torch.int32, device=scores.device)
+    _need(topk_idx, "topk_idx", (torch.int32,), (B, Q, k))
+    if workspace is None:
+        workspace = torch.zeros(WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=scores.device)
+    st = load().dsa_indexer_topk_mtp(_ptr(scores), _ptr(seq_lens), B, Q, max_context, k, _ptr(topk_idx),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(scores.device))
+    _check(st, "dsa_indexer_topk_mtp")
+    return topk_idx
+
+
+def dsa_indexer_fused_mtp(q, w, key_pool, page_table, seq_lens, max_context: int, k: int, topk_idx=None,
+                          scores=None, workspace=None):
+    """Scores + top-k for next_n query tokens per request; ``scores`` None keeps the rows unwritten."""
+    B, Q = _mtp_args(q, w, key_pool, page_table, seq_lens, max_context)
+    if topk_idx is None:
+        topk_idx = torch.empty((B, Q, k), dtype=torch.int32, device=q.device)
+    _need(topk_idx, "topk_idx", (torch.int32,), (B, Q, k))
+    if scores is not None:
+        _need(scores, "scores", (torch.float32,), (B, Q, max_context // 4))
+    if workspace is None:
+        n = workspace_size_mtp(B, Q, max_context, k)
+        if n == 0:
+            raise ValueError("invalid shape for a workspace")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    st = load().dsa_indexer_fused_mtp(_ptr(q), _ptr(w), _ptr(key_pool), key_pool.shape[0], _ptr(page_table),
+                                      _ptr(seq_lens), B, Q, max_context, k, _ptr(topk_idx), _ptr(scores),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(q.device))
+    _check(st, "dsa_indexer_fused_mtp")
     return topk_idx
 
 

@@ -85,13 +85,13 @@ dsa_status_t make_codes_map(CUtensorMap* codes_map, const void* key_codes, int64
     return DSA_OK;
 }
 
-// Query [batch * 32, 64] bf16; one box = the 32 heads of one request.
-dsa_status_t make_q_map(CUtensorMap* map, const void* q, int32_t batch) {
+// Query [batch * tokens * 32, 64] bf16; one box = the tokens x 32 heads of one request.
+dsa_status_t make_q_map(CUtensorMap* map, const void* q, int32_t batch, int32_t tokens = 1) {
     auto enc = encode_tiled();
     if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled lookup");
-    const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), cuuint64_t(batch) * kHeads};
+    const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), cuuint64_t(batch) * cuuint64_t(tokens) * kHeads};
     const cuuint64_t strides[1] = {cuuint64_t(kHeadDim * 2)};
-    const cuuint32_t box[2] = {cuuint32_t(kHeadDim), cuuint32_t(kHeads)};
+    const cuuint32_t box[2] = {cuuint32_t(kHeadDim), cuuint32_t(kHeads * tokens)};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box,
                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -159,7 +159,7 @@ dsa_status_t check_score_inputs(const void* q, const float* w, const void* key_p
 
 dsa::ScoresParams score_params(const float* w, int64_t num_pages, const int32_t* page_table,
                                const int32_t* seq_lens, int32_t batch, int64_t max_context, float* out,
-                               int fill_dead, void* workspace) {
+                               int fill_dead, void* workspace, int32_t tokens = 1) {
     dsa::ScoresParams p{};
     p.page_table = page_table;
     p.seq_lens = seq_lens;
@@ -172,19 +172,20 @@ dsa::ScoresParams score_params(const float* w, int64_t num_pages, const int32_t*
     p.table_width = int32_t(max_context / DSA_PAGE_TOKENS);
     p.batch = batch;
     p.fill_dead = fill_dead;
+    p.tokens = tokens;
     return p;
 }
 
 dsa_status_t run_scores(const void* q, const float* w, const void* key_pool, int64_t num_pages,
                         const int32_t* page_table, const int32_t* seq_lens, int32_t batch, int64_t max_context,
-                        float* out, int fill_dead, void* workspace, cudaStream_t stream) {
+                        float* out, int fill_dead, void* workspace, cudaStream_t stream, int32_t tokens = 1) {
     CUtensorMap keys_map, q_map;
     dsa_status_t st = make_keys_map(&keys_map, key_pool, num_pages);
     if (st != DSA_OK) return st;
-    st = make_q_map(&q_map, q, batch);
+    st = make_q_map(&q_map, q, batch, tokens);
     if (st != DSA_OK) return st;
     const dsa::ScoresParams p =
-        score_params(w, num_pages, page_table, seq_lens, batch, max_context, out, fill_dead, workspace);
+        score_params(w, num_pages, page_table, seq_lens, batch, max_context, out, fill_dead, workspace, tokens);
     const cudaError_t e = dsa::launch_scores(keys_map, q_map, p, stream);
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "scores kernel launch");
 }
@@ -205,7 +206,7 @@ dsa_status_t run_scores_fp8(const void* q, const float* w, const void* key_codes
 }
 
 dsa_status_t run_topk(const float* scores, const int32_t* seq_lens, int32_t batch, int64_t max_context, int32_t k,
-                      int32_t* topk_idx, void* workspace, cudaStream_t stream) {
+                      int32_t* topk_idx, void* workspace, cudaStream_t stream, int32_t tokens = 1) {
     dsa::TopkParams p{};
     p.scores = scores;
     p.seq_lens = seq_lens;
@@ -215,6 +216,7 @@ dsa_status_t run_topk(const float* scores, const int32_t* seq_lens, int32_t batc
     p.row_width = max_context / 4;
     p.batch = batch;
     p.k = k;
+    p.tokens = tokens;
     const cudaError_t e = dsa::launch_topk(p, stream);
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "top-k kernel launch");
 }
@@ -325,6 +327,68 @@ dsa_status_t dsa_indexer_fused_fp8(const void* q, const float* w, const void* ke
                         scores_opt ? 1 : 0, workspace, s);
     if (st != DSA_OK) return st;
     return run_topk(rows, seq_lens, batch, max_context, k, topk_idx, workspace, s);
+}
+
+size_t dsa_indexer_workspace_size_mtp(int32_t batch, int32_t next_n, int64_t max_context, int32_t k) {
+    (void)k;
+    if (check_shape(batch, max_context) != DSA_OK || next_n < 1 || next_n > DSA_MAX_NEXT_N) return 0;
+    return dsa::kWorkspaceHeaderBytes + size_t(batch) * size_t(next_n) * size_t(max_context / 4) * sizeof(float);
+}
+
+dsa_status_t dsa_indexer_scores_mtp(const void* q, const float* w, const void* key_pool, int64_t num_pages,
+                                    const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                                    int32_t next_n, int64_t max_context, float* scores, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    dsa_status_t st = check_shape(batch, max_context);
+    if (st != DSA_OK) return st;
+    if (next_n < 1 || next_n > DSA_MAX_NEXT_N) return DSA_ERR_INVALID_ARG;
+    st = check_score_inputs(q, w, key_pool, num_pages, page_table, seq_lens);
+    if (st != DSA_OK) return st;
+    if (!scores || !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
+    st = check_workspace(workspace, workspace_bytes, dsa::kWorkspaceHeaderBytes);
+    if (st != DSA_OK) return st;
+    return run_scores(q, w, key_pool, num_pages, page_table, seq_lens, batch, max_context, scores, 1, workspace,
+                      static_cast<cudaStream_t>(stream), next_n);
+}
+
+dsa_status_t dsa_indexer_topk_mtp(const float* scores, const int32_t* seq_lens, int32_t batch, int32_t next_n,
+                                  int64_t max_context, int32_t k, int32_t* topk_idx, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    dsa_status_t st = check_shape(batch, max_context);
+    if (st != DSA_OK) return st;
+    if (next_n < 1 || next_n > DSA_MAX_NEXT_N) return DSA_ERR_INVALID_ARG;
+    if (!scores || !seq_lens || !topk_idx || !aligned(scores, 16) || !aligned(seq_lens, 4) || !aligned(topk_idx, 4))
+        return DSA_ERR_INVALID_ARG;
+    if (k < 1 || int64_t(k) > max_context / 4) return DSA_ERR_INVALID_ARG;
+    st = check_workspace(workspace, workspace_bytes, dsa::kWorkspaceHeaderBytes);
+    if (st != DSA_OK) return st;
+    return run_topk(scores, seq_lens, batch, max_context, k, topk_idx, workspace, static_cast<cudaStream_t>(stream),
+                    next_n);
+}
+
+dsa_status_t dsa_indexer_fused_mtp(const void* q, const float* w, const void* key_pool, int64_t num_pages,
+                                   const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                                   int32_t next_n, int64_t max_context, int32_t k, int32_t* topk_idx,
+                                   float* scores_opt, void* workspace, size_t workspace_bytes, void* stream) {
+    dsa_status_t st = check_shape(batch, max_context);
+    if (st != DSA_OK) return st;
+    if (next_n < 1 || next_n > DSA_MAX_NEXT_N) return DSA_ERR_INVALID_ARG;
+    st = check_score_inputs(q, w, key_pool, num_pages, page_table, seq_lens);
+    if (st != DSA_OK) return st;
+    if (!topk_idx || !aligned(topk_idx, 4)) return DSA_ERR_INVALID_ARG;
+    if (scores_opt && !aligned(scores_opt, 16)) return DSA_ERR_INVALID_ARG;
+    if (k < 1 || int64_t(k) > max_context / 4) return DSA_ERR_INVALID_ARG;
+    const size_t need =
+        scores_opt ? dsa::kWorkspaceHeaderBytes : dsa_indexer_workspace_size_mtp(batch, next_n, max_context, k);
+    st = check_workspace(workspace, workspace_bytes, need);
+    if (st != DSA_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* rows = scores_opt ? scores_opt
+                             : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kWorkspaceHeaderBytes);
+    st = run_scores(q, w, key_pool, num_pages, page_table, seq_lens, batch, max_context, rows, scores_opt ? 1 : 0,
+                    workspace, s, next_n);
+    if (st != DSA_OK) return st;
+    return run_topk(rows, seq_lens, batch, max_context, k, topk_idx, workspace, s, next_n);
 }
 
 dsa_status_t dsa_indexer_get_error(void* workspace, uint32_t* code, int clear, void* stream) {

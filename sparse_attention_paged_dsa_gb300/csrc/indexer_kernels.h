@@ -37,18 +37,20 @@ struct ScoresParams {
     int32_t table_width;        // max_context / 256
     int32_t batch;
     int32_t fill_dead;          // 1: write -inf from the live extent to the row end
+    int32_t tokens;             // query tokens per request (q [batch, tokens, 32, 64], rows batch x tokens)
     const float* key_scales;    // [num_pages, 64] per-key scales of the fp8 cache (fp8 kernel only)
 };
 
 struct TopkParams {
-    const float* scores;  // [batch, row_width]
-    const int32_t* seq_lens;
-    int32_t* out;         // [batch, k]
+    const float* scores;  // [batch x tokens, row_width]
+    const int32_t* seq_lens;  // [batch]
+    int32_t* out;         // [batch x tokens, k]
     uint32_t* err;
     int64_t max_context;
     int64_t row_width;
     int32_t batch;
     int32_t k;
+    int32_t tokens;       // query tokens per request: row r is token r % tokens of request r / tokens
 };
 
 // Scores kernel: persistent, one CTA per SM, TMA page gather + tcgen05 QK.

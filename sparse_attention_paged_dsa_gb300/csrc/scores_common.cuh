@@ -141,9 +141,11 @@ struct UnitSchedule {
     }
 };
 
-// Stream -inf over every row's positions past its live units, rows split over
-// all CTAs (threads et in [0, nthreads) of each CTA take part).
-__device__ __forceinline__ void fill_dead_tails(const RowTable& t, const ScoresParams& p, int et, int nthreads) {
+// Stream -inf over every row's positions past its request's live units (all
+// `tokens` rows of a request share the extent), rows split over all CTAs
+// (threads et in [0, nthreads) of each CTA take part).
+__device__ __forceinline__ void fill_dead_tails(const RowTable& t, const ScoresParams& p, int et, int nthreads,
+                                                int tokens = 1) {
     const int64_t M = p.row_width;
     const float neg_inf = __int_as_float(0xff800000);
     const float4 ninf4 = make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
@@ -151,9 +153,11 @@ __device__ __forceinline__ void fill_dead_tails(const RowTable& t, const ScoresP
     for (int b = 0; b < p.batch; ++b) {
         const int64_t units = t.unit_start[b + 1] - t.unit_start[b];
         const int64_t extent = units * kUnitPositions < M ? units * kUnitPositions : M;
-        float4* row = reinterpret_cast<float4*>(p.out + int64_t(b) * M);
-        for (int64_t i = extent / 4 + int64_t(blockIdx.x) * nthreads + et; i < M / 4; i += stride)
-            __stcs(row + i, ninf4);
+        for (int j = 0; j < tokens; ++j) {
+            float4* row = reinterpret_cast<float4*>(p.out + (int64_t(b) * tokens + j) * M);
+            for (int64_t i = extent / 4 + int64_t(blockIdx.x) * nthreads + et; i < M / 4; i += stride)
+                __stcs(row + i, ninf4);
+        }
     }
 }
 

@@ -17,10 +17,15 @@
 //     same grid as an 8K one.
 //   * Work unit = 2 consecutive pages of one request = 128 keys = 16 KiB.
 //     Each CTA takes an equal contiguous range of floor(U / grid) of the
-//     batch's U live units (few request changes per CTA); the fewer than
-//     `grid` units left over go one at a time to whichever CTAs ask first,
-//     from a counter in the workspace header.  The last CTA to leave resets
-//     the counter.  Cost is O(live units), not O(max_context).
+//     batch's U live units (few request changes per CTA), plus at most one of
+//     the fewer than `grid` units left over; the schedule is fixed by U, the
+//     grid and the CTA index.  Cost is O(live units), not O(max_context).
+//   * Q query tokens per request (Q = 1 for the plain decode step; 2..4 for
+//     multi-token decoding, row f3): the request's Q x 32 query heads form
+//     the N = 32 Q side of one MMA per unit, so the key bytes are read once
+//     for all Q tokens; token j of a request with seq_len L scores the
+//     ceil((L - (Q - 1 - j)) / 4) keys of its own causal prefix and writes
+//     row b Q + j.
 //   * Two producer warps (one lane each issues) gather pages with TMA tiled
 //     loads (128-byte swizzle) into a kStages ring of 16 KiB stages: warp 0
 //     the CTA's even units, warp 2 the odd ones.  One issuing thread keeps
@@ -29,9 +34,10 @@
 //     is loaded once per request change into a small ring of its own.  Each
 //     unit's request, page pair and page validity go to a small metadata
 //     ring.
-//   * Warp 1 (one lane) issues tcgen05.mma kind::f16, M=128 keys x N=32 heads
-//     x K=64 dims (4 instructions of K=16) into one of 4 TMEM accumulators of
-//     32 fp32 columns, then publishes the accumulator and the unit's metadata.
+//   * Warp 1 (one lane) issues tcgen05.mma kind::f16, M=128 keys x N=32 Q
+//     heads x K=64 dims (4 instructions of K=16) into one of kAccStages TMEM
+//     accumulators of 32 Q fp32 columns, then publishes the accumulator and
+//     the unit's metadata.
 //   * kEpiGroups groups of 4 warps (group g takes every kEpiGroups-th unit)
 //     read the accumulators with tcgen05.ld (thread = key row, registers =
 //     32 heads), apply relu, the head weights and the head sum in registers,
@@ -58,51 +64,71 @@ namespace {
 
 using namespace scores;
 
-// Three CTAs per SM, two TMA-issuing producer warps each: one issuing thread
-// keeps too few page boxes in flight to cover HBM latency (a TMA instruction
-// takes about 120 cycles to issue), so each SM runs six issuers.
-constexpr int kStages = 3;                             // 16 KiB stages per CTA, shared by the producer warps
-constexpr int kEpiGroups = 1;                          // epilogue groups of 4 warps
-constexpr int kCtasPerSm = 3;
-constexpr int kQSlots = 2;
-constexpr int kAccStages = 4;
-constexpr int kMetaRing = 16;                          // >= kStages + kAccStages + 1
-constexpr int kAccCols = 32;                           // fp32 columns per accumulator (N = 32 heads)
-constexpr uint32_t kTmemCols = kAccStages * kAccCols;  // 128 (power of two >= 32)
-constexpr int kEpiThreads = 128 * kEpiGroups;
-constexpr int kThreads = 128 + kEpiThreads;           // producers 0 and 2, MMA 1, set-up 3, epilogue 4..
-constexpr int kStageBytes = 2 * kPageBytes;            // 16 KiB: 128 keys x 128 B
-constexpr uint32_t kIdesc = idesc_bf16_f32(128, kAccCols);
-static_assert(kAccStages % kEpiGroups == 0, "each epilogue group owns whole accumulator stages");
-static_assert(kMetaRing >= kStages + kAccStages + 1, "metadata ring too small");
+// Per query-token count Q.  Q = 1: three CTAs per SM, two TMA-issuing
+// producer warps each: one issuing thread keeps too few page boxes in flight
+// to cover HBM latency (a TMA instruction takes about 120 cycles to issue),
+// so each SM runs six issuers.  Q >= 2: the Q x 4 KiB query tiles and the
+// 32 Q-column accumulators need two CTAs per SM.
+template <int Q>
+struct Cfg {
+    static constexpr int kCtasPerSm = Q == 1 ? 3 : 2;
+    static constexpr int kStages = Q == 1 ? 3 : 4;           // 16 KiB stages per CTA, shared by the producers
+    static constexpr int kEpiGroups = 1;                      // epilogue groups of 4 warps
+    static constexpr int kQSlots = 2;
+    static constexpr int kAccStages = Q <= 2 ? 4 : 2;
+    static constexpr int kMetaRing = 16;                      // >= kStages + kAccStages + 1
+    static constexpr int kAccCols = 32 * Q;                   // fp32 columns per accumulator (N = 32 Q heads)
+    static constexpr uint32_t kTmemCols =                     // power of two >= 32
+        kAccStages * kAccCols <= 128 ? 128u : 256u;
+    static constexpr int kEpiThreads = 128 * kEpiGroups;
+    static constexpr int kThreads = 128 + kEpiThreads;       // producers 0 and 2, MMA 1, set-up 3, epilogue 4..
+    static constexpr int kStageBytes = 2 * kPageBytes;        // 16 KiB: 128 keys x 128 B
+    static constexpr int kQTileBytes = Q * kQRowBytes;        // Q tokens x 32 heads x 64 dims of bf16
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(128, kAccCols);
+    static_assert(kAccStages % kEpiGroups == 0, "each epilogue group owns whole accumulator stages");
+    static_assert(kMetaRing >= kStages + kAccStages + 1, "metadata ring too small");
+    static_assert(kAccStages * kAccCols <= int(kTmemCols), "accumulators fit the allocation");
+    static_assert(int(kTmemCols) * kCtasPerSm <= 512, "TMEM columns per SM");
+};
 
-struct __align__(8) SmemCtl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t qfull[kQSlots];
-    uint64_t qempty[kQSlots];
-    uint64_t tfull[kAccStages];
-    uint64_t tempty[kAccStages];
-    uint64_t tmeta[kAccStages];
+template <int Q>
+struct __align__(16) SmemCtl {
+    uint64_t full[Cfg<Q>::kStages];
+    uint64_t empty[Cfg<Q>::kStages];
+    uint64_t qfull[Cfg<Q>::kQSlots];
+    uint64_t qempty[Cfg<Q>::kQSlots];
+    uint64_t tfull[Cfg<Q>::kAccStages];
+    uint64_t tempty[Cfg<Q>::kAccStages];
+    uint64_t tmeta[Cfg<Q>::kAccStages];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    int32_t meta[kMetaRing];
+    int32_t meta[Cfg<Q>::kMetaRing];
+    __align__(16) float wtok[4][Q > 1 ? Q : 1][kHeads];  // Q > 1: each epilogue warp's copy of the request's head weights
     RowTable rows;
 };
 
-constexpr size_t kTileBytes = size_t(kStages) * kStageBytes + size_t(kQSlots) * kQRowBytes;
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes + sizeof(SmemCtl);
-static_assert(kSmemBytes * kCtasPerSm <= 228 * 1024, "shared memory budget per SM");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget per CTA");
+template <int Q>
+struct Layout {
+    static constexpr size_t kTileBytes =
+        size_t(Cfg<Q>::kStages) * Cfg<Q>::kStageBytes + size_t(Cfg<Q>::kQSlots) * Cfg<Q>::kQTileBytes;
+    static constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes + sizeof(SmemCtl<Q>);
+    static_assert(kSmemBytes * Cfg<Q>::kCtasPerSm <= 226 * 1024, "shared memory budget per SM");
+};
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+template <int Q>
+__global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
     scores_kernel(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CUtensorMap q_map,
                   const ScoresParams p) {
+    using C = Cfg<Q>;
+    constexpr int kStages = C::kStages, kEpiGroups = C::kEpiGroups, kQSlots = C::kQSlots;
+    constexpr int kAccStages = C::kAccStages, kMetaRing = C::kMetaRing, kAccCols = C::kAccCols;
+    constexpr int kEpiThreads = C::kEpiThreads, kStageBytes = C::kStageBytes, kQTileBytes = C::kQTileBytes;
+    constexpr uint32_t kTmemCols = C::kTmemCols, kIdesc = C::kIdesc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* qtiles = tiles + size_t(kStages) * kStageBytes;
-    SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(tiles + kTileBytes);
+    SmemCtl<Q>& ctl = *reinterpret_cast<SmemCtl<Q>*>(tiles + Layout<Q>::kTileBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -186,9 +212,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         if (!mbar_wait(&ctl.qempty[qs], ((k / kQSlots) & 1) ^ 1u, &ctl.abort)) {
                             failed = 1;
                         } else {
-                            mbar_arrive_expect_tx(&ctl.qfull[qs], kQRowBytes);
-                            tma_load_2d(qtiles + size_t(qs) * kQRowBytes, &q_map, &ctl.qfull[qs], 0, bi * kHeads,
-                                        pol_q);
+                            mbar_arrive_expect_tx(&ctl.qfull[qs], kQTileBytes);
+                            tma_load_2d(qtiles + size_t(qs) * kQTileBytes, &q_map, &ctl.qfull[qs], 0,
+                                        bi * Q * kHeads, pol_q);
 #pragma unroll
                             for (int j = 0; j + 1 < kQSlots; ++j) q_mine[j] = q_mine[j + 1];
                             q_mine[kQSlots - 1] = k;
@@ -280,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     tc_fence_after_sync();
                     const uint64_t a_desc = smem_desc_kmajor_sw128(smem_u32(tiles + size_t(stage) * kStageBytes));
                     const uint64_t b_desc =
-                        smem_desc_kmajor_sw128(smem_u32(qtiles + size_t(q_used % kQSlots) * kQRowBytes));
+                        smem_desc_kmajor_sw128(smem_u32(qtiles + size_t(q_used % kQSlots) * kQTileBytes));
                     const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
 #pragma unroll
                     for (int kk = 0; kk < kHeadDim / 16; ++kk)  // K = 16 per MMA: +32 bytes = +2 in the address field
@@ -316,12 +342,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int quad = warp & 3;          // TMEM lanes [32*quad, 32*quad + 32)
         const float neg_inf = __int_as_float(0xff800000);
 
-        if (p.fill_dead) fill_dead_tails(ctl.rows, p, et, kEpiThreads);
+        if (p.fill_dead) fill_dead_tails(ctl.rows, p, et, kEpiThreads, Q);
 
         int cur_b = -1, n = 0;
-        float wv[kHeads];
+        int n_tok[Q];  // live keys of each token of the current request
+        float wv[Q == 1 ? kHeads : 1];
 #pragma unroll
-        for (int h = 0; h < kHeads; ++h) wv[h] = 0.f;
+        for (int h = 0; h < (Q == 1 ? kHeads : 1); ++h) wv[h] = 0.f;
+#pragma unroll
+        for (int j = 0; j < Q; ++j) n_tok[j] = 0;
         bool stop = false;
         for (int i = group;; i += kEpiGroups) {
             const int acc = i % kAccStages;
@@ -336,14 +365,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const int pair = meta_pair(m);
             const bool page_ok = (m >> (quad >> 1)) & 1;  // quadrants 0-1: first page, 2-3: second
             if (b != cur_b) {
-                const float4* wr = reinterpret_cast<const float4*>(p.w + int64_t(b) * kHeads);
+                if constexpr (Q == 1) {
+                    const float4* wr = reinterpret_cast<const float4*>(p.w + int64_t(b) * kHeads);
 #pragma unroll
-                for (int h4 = 0; h4 < kHeads / 4; ++h4) {
-                    const float4 v = __ldg(wr + h4);
-                    wv[4 * h4 + 0] = v.x;
-                    wv[4 * h4 + 1] = v.y;
-                    wv[4 * h4 + 2] = v.z;
-                    wv[4 * h4 + 3] = v.w;
+                    for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+                        const float4 v = __ldg(wr + h4);
+                        wv[4 * h4 + 0] = v.x;
+                        wv[4 * h4 + 1] = v.y;
+                        wv[4 * h4 + 2] = v.z;
+                        wv[4 * h4 + 3] = v.w;
+                    }
+                    n_tok[0] = ctl.rows.n_live[b];
+                } else {  // this warp's copy of the Q x 32 head weights; per-token causal lengths
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < Q; ++j) ctl.wtok[quad][j][lane] = __ldg(p.w + (int64_t(b) * Q + j) * kHeads + lane);
+                    __syncwarp();
+                    int64_t L = p.seq_lens[b];
+                    L = L < 0 ? 0 : (L > p.max_context ? p.max_context : L);
+#pragma unroll
+                    for (int j = 0; j < Q; ++j) {
+                        const int64_t Lj = L - (Q - 1 - j);
+                        n_tok[j] = Lj > 0 ? int((Lj + 3) >> 2) : 0;
+                    }
                 }
                 n = ctl.rows.n_live[b];
                 cur_b = b;
@@ -354,23 +398,49 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 break;
             }
             tc_fence_after_sync();
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * kAccCols), r);
-            tmem_ld_wait(r);
-            tc_fence_before_sync();
-            mbar_arrive(&ctl.tempty[acc]);
-
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-            for (int h = 0; h < kHeads; h += 4) {
-                s0 = fmaf(wv[h + 0], fmaxf(__uint_as_float(r[h + 0]), 0.f), s0);
-                s1 = fmaf(wv[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
-                s2 = fmaf(wv[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
-                s3 = fmaf(wv[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
-            }
-            const float s = (s0 + s1) + (s2 + s3);
             const int64_t t = int64_t(pair) * kUnitPositions + quad * 32 + lane;
-            if (t < M) p.out[int64_t(b) * M + t] = (t < n && page_ok) ? s : neg_inf;
+            const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * kAccCols);
+            if constexpr (Q == 1) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr, r);
+                tmem_ld_wait(r);
+                tc_fence_before_sync();
+                mbar_arrive(&ctl.tempty[acc]);
+
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                for (int h = 0; h < kHeads; h += 4) {
+                    s0 = fmaf(wv[h + 0], fmaxf(__uint_as_float(r[h + 0]), 0.f), s0);
+                    s1 = fmaf(wv[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
+                    s2 = fmaf(wv[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
+                    s3 = fmaf(wv[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
+                }
+                const float s = (s0 + s1) + (s2 + s3);
+                if (t < M) p.out[int64_t(b) * M + t] = (t < n && page_ok) ? s : neg_inf;
+            } else {
+#pragma unroll 1
+                for (int j = 0; j < Q; ++j) {  // token j: accumulator columns [32 j, 32 j + 32)
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + uint32_t(32 * j), r);
+                    tmem_ld_wait(r);
+                    if (j == Q - 1) {
+                        tc_fence_before_sync();
+                        mbar_arrive(&ctl.tempty[acc]);
+                    }
+                    const float4* wr = reinterpret_cast<const float4*>(ctl.wtok[quad][j]);
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                    for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+                        const float4 wq = wr[h4];
+                        s0 = fmaf(wq.x, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f), s0);
+                        s1 = fmaf(wq.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), s1);
+                        s2 = fmaf(wq.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), s2);
+                        s3 = fmaf(wq.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), s3);
+                    }
+                    const float s = (s0 + s1) + (s2 + s3);
+                    if (t < M) p.out[(int64_t(b) * Q + j) * M + t] = (t < n_tok[j] && page_ok) ? s : neg_inf;
+                }
+            }
         }
         if (stop && lane == 0) {
             atomicOr(p.err, kErrWaitTimeout);
@@ -386,17 +456,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 }
 
-}  // namespace
-
-cudaError_t launch_scores(const CUtensorMap& keys_map, const CUtensorMap& q_map, const ScoresParams& p,
-                          cudaStream_t stream) {
+template <int Q>
+cudaError_t launch_scores_q(const CUtensorMap& keys_map, const CUtensorMap& q_map, const ScoresParams& p,
+                            cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+        e = cudaFuncSetAttribute(scores_kernel<Q>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(Layout<Q>::kSmemBytes));
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
@@ -404,16 +474,29 @@ cudaError_t launch_scores(const CUtensorMap& keys_map, const CUtensorMap& q_map,
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(sms * kCtasPerSm));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.gridDim = dim3(unsigned(sms * Cfg<Q>::kCtasPerSm));
+    cfg.blockDim = dim3(Cfg<Q>::kThreads);
+    cfg.dynamicSmemBytes = Layout<Q>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, scores_kernel, keys_map, q_map, p);
+    return cudaLaunchKernelEx(&cfg, scores_kernel<Q>, keys_map, q_map, p);
+}
+
+}  // namespace
+
+cudaError_t launch_scores(const CUtensorMap& keys_map, const CUtensorMap& q_map, const ScoresParams& p,
+                          cudaStream_t stream) {
+    switch (p.tokens) {
+        case 1: return launch_scores_q<1>(keys_map, q_map, p, stream);
+        case 2: return launch_scores_q<2>(keys_map, q_map, p, stream);
+        case 3: return launch_scores_q<3>(keys_map, q_map, p, stream);
+        case 4: return launch_scores_q<4>(keys_map, q_map, p, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace dsa

@@ -537,9 +537,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
     // results before touching global memory.
     pdl_wait_prior_grid();
     pdl_allow_next_grid();
-    const int b = blockIdx.x;
-    int64_t s = p.seq_lens[b];
+    const int b = blockIdx.x;  // row: request b / tokens, query token b % tokens
+    int64_t s = p.seq_lens[b / p.tokens];
     s = s < 0 ? 0 : (s > p.max_context ? p.max_context : s);
+    s -= p.tokens - 1 - b % p.tokens;  // token j sees the first L - (tokens - 1 - j) tokens
+    s = s < 0 ? 0 : s;
     const int n = int((s + 3) >> 2);
     const int k = p.k;
     int32_t* out = p.out + int64_t(b) * k;
@@ -579,7 +581,7 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
         configured[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(p.batch));
+    cfg.gridDim = dim3(unsigned(p.batch) * unsigned(p.tokens));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

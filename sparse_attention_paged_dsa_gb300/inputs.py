@@ -253,6 +253,33 @@ def with_fp8_keys(case: IndexerCase, scale: str = "absmax") -> IndexerCase:
                                key_scales=np.ascontiguousarray(sc))
 
 
+def with_next_n(case: IndexerCase, next_n: int, dist: str = "normal") -> IndexerCase:
+    """The same keys, table and lengths with next_n query tokens per request.
+
+    q becomes [B, next_n, 32, 64] and w [B, next_n, 32]; the last token keeps the case's own q
+    and w, the others are fresh draws from the stream [seed, 2]: q ~ N(0,1) -> bf16 and
+    w ~ N(0, 1/32) ("normal"), or integer q in [-4, 4] and w = +-2^-j, j in 1..4 ("int", for
+    cases made with key_dist="int").  The request's seq_len counts all next_n tokens."""
+    if next_n == 1:
+        return dataclasses.replace(case, q=case.q[:, None].copy(), w=case.w[:, None].copy())
+    rng = np.random.default_rng([case.seed, 2])
+    B = case.batch
+    q = np.empty((B, next_n) + case.q.shape[1:], dtype=case.q.dtype)
+    w = np.empty((B, next_n) + case.w.shape[1:], dtype=case.w.dtype)
+    q[:, -1] = case.q
+    w[:, -1] = case.w
+    for j in range(next_n - 1):
+        if dist == "int":
+            q[:, j] = _int_bf16(rng, case.q.shape, -4, 4)
+            sgn = rng.choice(np.array([-1.0, 1.0]), size=case.w.shape)
+            w[:, j] = (sgn * np.ldexp(1.0, -rng.integers(1, 5, size=case.w.shape))).astype(np.float32)
+        else:
+            q[:, j] = _normal_bf16(rng, case.q.shape)
+            w[:, j] = (rng.standard_normal(case.w.shape) * math.sqrt(1.0 / 32.0)).astype(np.float32)
+    return dataclasses.replace(case, name=f"{case.name}_q{next_n}", q=np.ascontiguousarray(q),
+                               w=np.ascontiguousarray(w))
+
+
 # The five workloads of the decode indexer, named by what they are.
 WORKLOADS = ("b1_ctx8k_seq512", "b16_ctx8k_mixed", "b64_ctx128k_loguniform",
              "b64_ctx1m_seq512", "b64_ctx128k_dense")
