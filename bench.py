@@ -63,6 +63,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-context-scaling", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the fp8 key-cache measurement")
     ap.add_argument("--no-mtp", action="store_true", help="skip the multi-token (next_n = 2, 4) measurement")
+    ap.add_argument("--no-proj", action="store_true", help="skip the q/w projection measurement")
+    ap.add_argument("--proj-d-model", type=int, default=7168, help="model width of the synthetic projection")
     ap.add_argument("--l2-flush", action="store_true",
                     help="memset a 512 MiB buffer before every timed launch (default: back-to-back steps; "
                          "the live keys are twice the L2)")
@@ -378,6 +380,34 @@ def run_mtp(args, case, binding, inputs, device, stream, live, pool, table, seq)
     return out
 
 
+def run_proj(args, binding, device, batch):
+    """q/w projection from a bf16 hidden state [batch, d] with synthetic weights (the pages give no shapes)."""
+    import torch
+    d = args.proj_d_model
+    g = torch.Generator(device="cpu").manual_seed(4242)
+    x = torch.randn((batch, d), generator=g).to(torch.bfloat16).to(device)
+    wq = (torch.randn((2048, d), generator=g) / d ** 0.5).to(torch.bfloat16).to(device)
+    ww = (torch.randn((32, d), generator=g) / d ** 0.5).to(torch.bfloat16).to(device)
+    q = torch.empty((batch, 32, 64), dtype=torch.bfloat16, device=device)
+    w = torch.empty((batch, 32), dtype=torch.float32, device=device)
+    ws = torch.zeros(binding.qw_proj_workspace_size(batch, d), dtype=torch.uint8, device=device)
+    fn = lambda: binding.dsa_indexer_qw_proj(x, wq, ww, q_out=q, w_out=w, workspace=ws)
+    for _ in range(5):
+        fn()
+    t = graph_us_per_call(fn) * 1e-6
+    if binding.get_error(ws) != 0:
+        raise RuntimeError("device error word set in the projection run")
+    wbytes = (2048 + 32) * d * 2
+    peak, peak_kind = measured_hbm_peak()
+    achieved = wbytes / t / 1e9
+    return {"value": batch / t, "unit": "tokens/s", "us_per_call": 1e6 * t, "batch": batch, "d_model": d,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "kernel": "proj_kernel", "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
+                         "algorithmic_bytes_per_launch": wbytes},
+            "timing": "CUDA-graph replay, 20 calls per graph, median of 20",
+            "weights": "synthetic N(0, 1/d) bf16: w_q [2048, d], w_w [32, d]; x N(0,1) bf16"}
+
+
 def workload_config(case, world, l2_flush=False):
     live = int(case.live_positions().sum())
     return {"workload": case.name, "batch": case.batch, "max_context": case.max_context,
@@ -508,6 +538,7 @@ def run_ours(args):
     fp8 = run_fp8(args, case, binding, inputs, device, stream, live) if not args.no_fp8 else None
     mtp = (run_mtp(args, case, binding, inputs, device, stream, live, pool, table, seq)
            if not args.no_mtp else None)
+    proj = run_proj(args, binding, device, case.batch) if not args.no_proj else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -544,6 +575,7 @@ def run_ours(args):
         "context_scaling": scaling_1m,
         "fp8_key_cache": fp8,
         "multi_token": mtp,
+        "qw_projection": proj,
         "e2e": e2e,
         "gpu_launches": 2 * n * world,
         "step": "dsa_indexer_fused with the full-width scores row (scores kernel, then top-k kernel)",

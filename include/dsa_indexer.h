@@ -240,6 +240,32 @@ DSA_API dsa_status_t dsa_indexer_fused_mtp(const void *q, const float *w, const 
                                    void *stream);
 
 /*
+ * The indexer's query / head-weight projection from the bf16 hidden state
+ * (row f4).  The pages replace forced-fp32 GEMMs on the indexer path by bf16
+ * tensor-core GEMMs fed the bf16 hidden state directly ("The Indexer
+ * O(max_context) Breakthrough", section "Phase 3: The FP32-to-bf16 GEMM
+ * Flip"); they give no weight shapes, so the model width is a parameter:
+ *     q[b, h, e] = sum_d x[b, d] * w_q[h * 64 + e, d]   -> bf16 (round to nearest even)
+ *     w[b, h]    = sum_d x[b, d] * w_w[h, d]            -> fp32
+ * with fp32 accumulation.  Layouts (C-contiguous, 16-byte aligned):
+ *     x      bf16 [batch, d_model]     (1 <= batch <= DSA_PROJ_MAX_TOKENS)
+ *     w_q    bf16 [32 * 64, d_model]   (d_model a multiple of 64, <= 65536)
+ *     w_w    bf16 [32, d_model]
+ *     q_out  bf16 [batch, 32, 64]      (the q layout of the indexer entry points)
+ *     w_out  fp32 [batch, 32]
+ * Workspace: dsa_indexer_qw_proj_workspace_size(batch, d_model) bytes (header
+ * plus fp32 partial sums).  The reduction over d is split across CTAs and
+ * summed in a fixed order: results are deterministic.
+ */
+#define DSA_PROJ_MAX_TOKENS 256
+
+DSA_API size_t dsa_indexer_qw_proj_workspace_size(int32_t batch, int64_t d_model);
+
+DSA_API dsa_status_t dsa_indexer_qw_proj(const void *x, const void *w_q, const void *w_w, int32_t batch,
+                                 int64_t d_model, void *q_out, float *w_out, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/*
  * Read the sticky device error word into *code (host pointer).  Synchronises
  * `stream` (not capture-safe).  clear != 0 zeroes the word afterwards.
  */

@@ -209,6 +209,24 @@ def case_scores_mtp(case) -> np.ndarray:
     return scores_mtp(case.q, case.w, case.key_pool, case.page_table, case.seq_lens, case.max_context)
 
 
+def qw_proj(x_bits, wq_bits, ww_bits):
+    """fp64 q [B, 32, 64] and w [B, 32] from the bf16 hidden state: q = x Wq^T, w = x Ww^T.
+
+    The bf16 bit patterns are widened exactly; the products and sums are fp64 (a
+    library matmul on fp64 arrays is the step)."""
+    x = _bf16_bits_to_f64(x_bits)
+    wq = _bf16_bits_to_f64(wq_bits)
+    ww = _bf16_bits_to_f64(ww_bits)
+    q = x @ wq.T
+    w = x @ ww.T
+    return q.reshape(x.shape[0], ww.shape[0], -1), w
+
+
+def _bf16_bits_to_f64(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
 def case_scores(case) -> np.ndarray:
     return scores(case.q, case.w, case.key_pool, case.page_table, case.seq_lens, case.max_context)
 

@@ -68,6 +68,10 @@ def load():
     lib.dsa_indexer_topk_mtp.restype = st
     lib.dsa_indexer_fused_mtp.argtypes = [p, p, p, i64, p, p, i32, i32, i64, i32, p, p, p, sz, p]
     lib.dsa_indexer_fused_mtp.restype = st
+    lib.dsa_indexer_qw_proj_workspace_size.argtypes = [i32, i64]
+    lib.dsa_indexer_qw_proj_workspace_size.restype = sz
+    lib.dsa_indexer_qw_proj.argtypes = [p, p, p, i32, i64, p, p, p, sz, p]
+    lib.dsa_indexer_qw_proj.restype = st
     lib.dsa_indexer_get_error.argtypes = [p, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, p]
     lib.dsa_indexer_get_error.restype = st
     lib.dsa_status_string.argtypes = [st]
@@ -308,6 +312,35 @@ def dsa_indexer_fused_mtp(q, w, key_pool, page_table, seq_lens, max_context: int
                                       _stream(q.device))
     _check(st, "dsa_indexer_fused_mtp")
     return topk_idx
+
+
+def qw_proj_workspace_size(batch: int, d_model: int) -> int:
+    return int(load().dsa_indexer_qw_proj_workspace_size(batch, d_model))
+
+
+def dsa_indexer_qw_proj(x, w_q, w_w, q_out=None, w_out=None, workspace=None):
+    """q [B, 32, 64] bf16 and w [B, 32] fp32 from the bf16 hidden state x [B, d] (fp32 accumulate)."""
+    if x.dim() != 2:
+        raise ValueError(f"x must be [batch, d_model], got {tuple(x.shape)}")
+    B, d = x.shape
+    _need(x, "x", _BF16, (B, d))
+    _need(w_q, "w_q", _BF16, (HEADS * HEAD_DIM, d))
+    _need(w_w, "w_w", _BF16, (HEADS, d))
+    if q_out is None:
+        q_out = torch.empty((B, HEADS, HEAD_DIM), dtype=torch.bfloat16, device=x.device)
+    _need(q_out, "q_out", _BF16, (B, HEADS, HEAD_DIM))
+    if w_out is None:
+        w_out = torch.empty((B, HEADS), dtype=torch.float32, device=x.device)
+    _need(w_out, "w_out", (torch.float32,), (B, HEADS))
+    if workspace is None:
+        n = qw_proj_workspace_size(B, d)
+        if n == 0:
+            raise ValueError("invalid shape for the projection")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=x.device)
+    st = load().dsa_indexer_qw_proj(_ptr(x), _ptr(w_q), _ptr(w_w), B, d, _ptr(q_out), _ptr(w_out), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(x.device))
+    _check(st, "dsa_indexer_qw_proj")
+    return q_out, w_out
 
 
 def get_error(workspace, clear: bool = True) -> int:

@@ -136,6 +136,30 @@ dsa_status_t make_plain_q_w_maps(CUtensorMap* q_map, CUtensorMap* w_map, const v
     return DSA_OK;
 }
 
+// bf16 2-D tensor [rows, cols] (cols contiguous) with a 128-byte-swizzled box of box_rows x 64.
+dsa_status_t make_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, uint32_t box_rows,
+                           const char* what) {
+    auto enc = encode_tiled();
+    if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled lookup");
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled(%s): CUresult %d", what,
+                      int(r));
+        return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+}
+
+constexpr int kProjMaxSplit = 8;  // CTAs per cluster (portable size)
+constexpr int kProjQTiles = (DSA_HEADS * DSA_HEAD_DIM) / 128;
+constexpr int64_t kProjMaxModel = 65536;
+
 dsa_status_t check_shape(int32_t batch, int64_t max_context) {
     if (batch < 1 || max_context < 1 || max_context % DSA_PAGE_TOKENS != 0) return DSA_ERR_INVALID_ARG;
     if (batch > DSA_MAX_BATCH || max_context > kMaxContext) return DSA_ERR_UNSUPPORTED;
@@ -389,6 +413,51 @@ dsa_status_t dsa_indexer_fused_mtp(const void* q, const float* w, const void* ke
                     workspace, s, next_n);
     if (st != DSA_OK) return st;
     return run_topk(rows, seq_lens, batch, max_context, k, topk_idx, workspace, s, next_n);
+}
+
+size_t dsa_indexer_qw_proj_workspace_size(int32_t batch, int64_t d_model) {
+    if (batch < 1 || batch > DSA_PROJ_MAX_TOKENS || d_model < 64 || d_model % 64 != 0 || d_model > kProjMaxModel)
+        return 0;
+    return dsa::kWorkspaceHeaderBytes;  // the error word only: partial sums stay on chip
+}
+
+dsa_status_t dsa_indexer_qw_proj(const void* x, const void* w_q, const void* w_w, int32_t batch, int64_t d_model,
+                                 void* q_out, float* w_out, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+    const size_t need = dsa_indexer_qw_proj_workspace_size(batch, d_model);
+    if (need == 0) return DSA_ERR_INVALID_ARG;
+    if (!x || !w_q || !w_w || !q_out || !w_out) return DSA_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w_q, 16) || !aligned(w_w, 16) || !aligned(q_out, 4) || !aligned(w_out, 4))
+        return DSA_ERR_INVALID_ARG;
+    dsa_status_t st = check_workspace(workspace, workspace_bytes, need);
+    if (st != DSA_OK) return st;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    const int atoms = int(d_model / 64);
+    int k_split = sms / (kProjQTiles + 1);  // about one weight-streaming CTA per SM
+    k_split = k_split < 1 ? 1 : (k_split > kProjMaxSplit ? kProjMaxSplit : k_split);
+    k_split = k_split > atoms ? atoms : k_split;
+    const int bp = dsa::proj_batch_pad(batch);
+    CUtensorMap wq_map, ww_map, x_map;
+    st = make_rows_map(&wq_map, w_q, kProjQTiles * 128, d_model, 128, "w_q");
+    if (st != DSA_OK) return st;
+    st = make_rows_map(&ww_map, w_w, DSA_HEADS, d_model, 128, "w_w");
+    if (st != DSA_OK) return st;
+    st = make_rows_map(&x_map, x, batch, d_model, uint32_t(bp), "x");
+    if (st != DSA_OK) return st;
+    dsa::ProjParams p{};
+    p.q_out = static_cast<__nv_bfloat16_raw*>(q_out);
+    p.w_out = w_out;
+    p.err = static_cast<uint32_t*>(workspace);
+    p.batch = batch;
+    p.batch_pad = bp;
+    p.d_model = int32_t(d_model);
+    p.q_tiles = kProjQTiles;
+    p.k_split = k_split;
+    e = dsa::launch_proj(wq_map, ww_map, x_map, p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "projection kernel launch");
 }
 
 dsa_status_t dsa_indexer_get_error(void* workspace, uint32_t* code, int clear, void* stream) {

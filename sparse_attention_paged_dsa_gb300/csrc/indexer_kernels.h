@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -66,5 +67,21 @@ cudaError_t launch_scores_fp8(const CUtensorMap& codes_map, const CUtensorMap& q
 
 // Top-k kernel: one CTA per request row, radix select over live positions.
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
+
+// Query / head-weight projection (split-K weight stream over a thread-block
+// cluster, deterministic reduction through distributed shared memory).
+struct ProjParams {
+    __nv_bfloat16_raw* q_out; // [batch, 32, 64] bf16
+    float* w_out;             // [batch, 32]
+    uint32_t* err;            // device error word
+    int32_t batch;
+    int32_t batch_pad;        // tokens padded to the MMA's N: 32, 64, 128 or 256
+    int32_t d_model;          // multiple of 64
+    int32_t q_tiles;          // 2048 / 128
+    int32_t k_split;          // CTAs along d (one cluster), 1..8, <= d_model / 64
+};
+int proj_batch_pad(int batch);
+cudaError_t launch_proj(const CUtensorMap& wq_map, const CUtensorMap& ww_map, const CUtensorMap& x_map,
+                        const ProjParams& p, cudaStream_t stream);
 
 }  // namespace dsa
