@@ -150,6 +150,33 @@ __device__ __forceinline__ void block_scan2(TopkSmem& sm, uint32_t a, uint32_t b
     b_before = sm.warp_eq[warp] + bi - b;
 }
 
+// --------------------------------------------------------------- short rows
+// k < n <= kSmallRow: every thread ranks its key against the whole row (equal
+// scores: lower position first); the k keys with rank < k are listed in
+// position order by one block scan.  A few hundred comparisons per thread and
+// two barriers, instead of the histogram passes.
+constexpr int kSmallRow = 256;
+
+__device__ __forceinline__ void select_row_small(TopkSmem& sm, uint32_t* keys, const float* __restrict__ row, int n,
+                                                 int k, int32_t* __restrict__ out) {
+    const int tid = threadIdx.x;
+    if (tid < n) keys[tid] = order_key(__ldcg(row + tid));
+    __syncthreads();
+    uint32_t sel = 0;
+    if (tid < n) {
+        const uint32_t me = keys[tid];
+        int rank = 0;
+        for (int j = 0; j < n; ++j) {
+            const uint32_t o = keys[j];
+            rank += (o > me || (o == me && j < tid)) ? 1 : 0;
+        }
+        sel = rank < k ? 1u : 0u;
+    }
+    uint32_t before, unused;
+    block_scan2(sm, sel, 0u, before, unused);
+    if (sel) out[before] = tid;
+}
+
 // ------------------------------------------------------------ register path
 // Shared-memory slot of position p: one pad word after every 32 keys, so that
 // thread i reading its key j hits bank (i + j) % 32.
@@ -550,6 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
         return;
     }
     const float* row = p.scores + int64_t(b) * p.row_width;
+    if (n <= kSmallRow) {
+        select_row_small(sm, cache, row, n, k, out);
+        return;
+    }
     if (n <= kRegCap && pad_slot(n) <= cache_cap) {
         if (!select_row_sampled(sm, cache, cache_cap, row, n, k, out)) {
             __syncthreads();
