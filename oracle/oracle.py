@@ -222,6 +222,50 @@ def qw_proj(x_bits, wq_bits, ww_bits):
     return q.reshape(x.shape[0], ww.shape[0], -1), w
 
 
+def sparse_mla_decode(q_bits, kv_bits, page_table, topk_idx, sm_scale: float, dv: int, seq_lens=None):
+    """fp64 sparse attention over the entries the indexer selected (multi-head latent decode).
+
+    Follows "The Indexer O(max_context) Breakthrough", section "Phase 1: The MMA Sparse-MLA
+    Decode Kernel" (attention restricted to the top-k cache entries the indexer picked, every
+    head reading the same gathered entries) with the head/entry shapes read as stated in the
+    design notes.  q [B, H, D] and the paged cache kv [P, E, D] are bf16 bit patterns (D = key
+    width; the value is the first dv dims of each entry); topk_idx [B, K] holds C4 positions.
+    Position t of request b is kv[page_table[b, t // E], t % E]; an entry is used when
+    0 <= t < ceil(seq_lens[b] / 4) (any t >= 0 when seq_lens is None), others (-1 padding)
+    are skipped.  For each request and head:
+        s_t = sm_scale * q_h . kv_t      over the request's used entries
+        o_h = sum_t softmax(s)_t kv_t[:dv],   lse_h = log sum_t exp(s_t)
+    A request with no used entry gives o = 0 and lse = -inf.  Also returns
+    o_abs = sum_t softmax(s)_t |kv_t[:dv]|, the scale of the rounding in a weighted sum.
+    Steps as written: gather, scaled dot products, max-shifted exponentials, normalised sums."""
+    q = _bf16_bits_to_f64(q_bits)
+    kv_bits = np.asarray(kv_bits)
+    table = np.asarray(page_table)
+    idx_all = np.asarray(topk_idx)
+    B, H, _ = q.shape
+    E = kv_bits.shape[1]
+    o = np.zeros((B, H, dv))
+    o_abs = np.zeros((B, H, dv))
+    lse = np.full((B, H), -np.inf)
+    for b in range(B):
+        idx = idx_all[b].astype(np.int64)
+        keep = idx >= 0
+        if seq_lens is not None:
+            keep &= idx < -(-int(seq_lens[b]) // 4)
+        idx = idx[keep]
+        if idx.size == 0:
+            continue
+        rows = _bf16_bits_to_f64(kv_bits[table[b, idx // E], idx % E])  # [n, D]
+        s = sm_scale * (q[b] @ rows.T)                                   # [H, n]
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
+        l = p.sum(axis=1, keepdims=True)
+        o[b] = (p @ rows[:, :dv]) / l
+        o_abs[b] = (p @ np.abs(rows[:, :dv])) / l
+        lse[b] = (m + np.log(l))[:, 0]
+    return o, lse, o_abs
+
+
 def _bf16_bits_to_f64(bits) -> np.ndarray:
     b = np.ascontiguousarray(bits, dtype=np.uint16)
     return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
