@@ -265,6 +265,45 @@ DSA_API dsa_status_t dsa_indexer_qw_proj(const void *x, const void *w_q, const v
                                  int64_t d_model, void *q_out, float *w_out, void *workspace,
                                  size_t workspace_bytes, void *stream);
 
+/* ---- Sparse multi-head latent attention decode over the top-k entries ----
+ *
+ * The attention step the indexer feeds ("The Indexer O(max_context)
+ * Breakthrough", sections "Phase 1: The MMA Sparse-MLA Decode Kernel" and
+ * "Phase 2: Split-K Parallelization"): for each request b and head h,
+ *     s_t     = sm_scale * q[b, h, :] . kv_t[:]          (576 dims)
+ *     o[b, h] = sum_t softmax_t(s) * kv_t[0:512]
+ *     lse[b,h]= log sum_t exp(s_t)
+ * over the entries t of topk_idx[b, :] that are used: 0 <= t < ceil(seq_len/4)
+ * (-1 padding and positions past the live length are skipped; a position given
+ * twice counts twice).  Entry t is kv_cache[page_table[b, t / 64], t % 64, :];
+ * the cache is paged exactly like the index keys (64 C4 entries per page).
+ * A request with no used entry gets o = 0 and lse = -inf.
+ *
+ *   q          [batch, 64, 576] bf16, device, 16-byte aligned
+ *   kv_cache   [num_pages, 64, 576] bf16, device, 16-byte aligned
+ *   page_table [batch, max_context / 256] int32; seq_lens [batch] int32 (tokens)
+ *   topk_idx   [batch, k] int32 C4 positions (the indexer's top-k rows), 1 <= k <= 2048
+ *   out        [batch, 64, 512] fp32; lse [batch, 64] fp32 (natural log), 16-byte aligned
+ *   workspace  >= dsa_sparse_mla_workspace_size(batch, k) bytes, 256-byte aligned,
+ *              header zeroed once (dsa_indexer_workspace_init); holds the error word
+ *              and the per-split partial outputs (sized for the current device).
+ * Asynchronous on `stream`; allocates nothing.  A live page id outside
+ * [0, num_pages) sets DSA_DEVERR_BAD_PAGE and that entry is read as zeros;
+ * results are unspecified while the error word is non-zero. */
+#define DSA_MLA_HEADS 64
+#define DSA_MLA_DIM 576
+#define DSA_MLA_DV 512
+#define DSA_MLA_MAX_TOPK 2048
+
+DSA_API size_t dsa_sparse_mla_workspace_size(int32_t batch, int32_t k);
+
+DSA_API dsa_status_t dsa_sparse_mla_decode(const void *q, const void *kv_cache, int64_t num_pages,
+                                           const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                                           int64_t max_context, const int32_t *topk_idx, int32_t k, float sm_scale,
+                                           float *out, float *lse, void *workspace, size_t workspace_bytes,
+                                           void *stream);
+
+
 /*
  * Read the sticky device error word into *code (host pointer).  Synchronises
  * `stream` (not capture-safe).  clear != 0 zeroes the word afterwards.

@@ -72,6 +72,10 @@ def load():
     lib.dsa_indexer_qw_proj_workspace_size.restype = sz
     lib.dsa_indexer_qw_proj.argtypes = [p, p, p, i32, i64, p, p, p, sz, p]
     lib.dsa_indexer_qw_proj.restype = st
+    lib.dsa_sparse_mla_workspace_size.argtypes = [i32, i32]
+    lib.dsa_sparse_mla_workspace_size.restype = sz
+    lib.dsa_sparse_mla_decode.argtypes = [p, p, i64, p, p, i32, i64, p, i32, ctypes.c_float, p, p, p, sz, p]
+    lib.dsa_sparse_mla_decode.restype = st
     lib.dsa_indexer_get_error.argtypes = [p, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, p]
     lib.dsa_indexer_get_error.restype = st
     lib.dsa_status_string.argtypes = [st]
@@ -341,6 +345,49 @@ def dsa_indexer_qw_proj(x, w_q, w_w, q_out=None, w_out=None, workspace=None):
                                     workspace.numel() * workspace.element_size(), _stream(x.device))
     _check(st, "dsa_indexer_qw_proj")
     return q_out, w_out
+
+
+MLA_HEADS, MLA_DIM, MLA_DV, MLA_MAX_TOPK = 64, 576, 512, 2048
+
+
+def sparse_mla_workspace_size(batch: int, k: int) -> int:
+    return int(load().dsa_sparse_mla_workspace_size(batch, k))
+
+
+def dsa_sparse_mla_decode(q, kv_cache, page_table, seq_lens, max_context: int, topk_idx, sm_scale: float,
+                          out=None, lse=None, workspace=None):
+    """o [B, 64, 512] fp32 and lse [B, 64] fp32: attention of q [B, 64, 576] bf16 over the
+    paged cache entries kv_cache [P, 64, 576] bf16 that topk_idx [B, k] selects."""
+    if q.dim() != 3:
+        raise ValueError(f"q must be [batch, 64, 576], got {tuple(q.shape)}")
+    B = q.shape[0]
+    _need(q, "q", _BF16, (B, MLA_HEADS, MLA_DIM))
+    _need(kv_cache, "kv_cache", _BF16)
+    if kv_cache.dim() != 3 or tuple(kv_cache.shape[1:]) != (PAGE_ENTRIES, MLA_DIM):
+        raise ValueError(f"kv_cache must be [num_pages, 64, 576], got {tuple(kv_cache.shape)}")
+    _need(page_table, "page_table", (torch.int32,), (B, max_context // PAGE_TOKENS))
+    _need(seq_lens, "seq_lens", (torch.int32,), (B,))
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != B:
+        raise ValueError(f"topk_idx must be [batch, k], got {tuple(topk_idx.shape)}")
+    k = topk_idx.shape[1]
+    _need(topk_idx, "topk_idx", (torch.int32,), (B, k))
+    if out is None:
+        out = torch.empty((B, MLA_HEADS, MLA_DV), dtype=torch.float32, device=q.device)
+    _need(out, "out", (torch.float32,), (B, MLA_HEADS, MLA_DV))
+    if lse is None:
+        lse = torch.empty((B, MLA_HEADS), dtype=torch.float32, device=q.device)
+    _need(lse, "lse", (torch.float32,), (B, MLA_HEADS))
+    if workspace is None:
+        n = sparse_mla_workspace_size(B, k)
+        if n == 0:
+            raise ValueError("invalid shape for the sparse MLA decode")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    st = load().dsa_sparse_mla_decode(_ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(page_table), _ptr(seq_lens),
+                                      B, max_context, _ptr(topk_idx), k, float(sm_scale), _ptr(out), _ptr(lse),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(q.device))
+    _check(st, "dsa_sparse_mla_decode")
+    return out, lse
 
 
 def get_error(workspace, clear: bool = True) -> int:

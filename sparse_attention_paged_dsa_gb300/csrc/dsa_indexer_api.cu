@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -243,6 +244,23 @@ dsa_status_t run_topk(const float* scores, const int32_t* seq_lens, int32_t batc
     p.tokens = tokens;
     const cudaError_t e = dsa::launch_topk(p, stream);
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "top-k kernel launch");
+}
+
+// Splits of a request's top-k row across CTAs (one CTA per SM): enough to fill
+// the current device once, at most one per 64-entry block and kMlaMaxSplits.
+int mla_splits(int32_t batch, int32_t k) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                   cudaSuccess)
+        sms = 148;
+    const int blocks = (k + 63) / 64;
+    int s = sms / batch;
+    if (s > blocks) s = blocks;
+    if (s > dsa::kMlaMaxSplits) s = dsa::kMlaMaxSplits;
+    return s < 1 ? 1 : s;
+}
+size_t mla_partial_floats(int32_t batch, int splits) {
+    return splits > 1 ? size_t(batch) * size_t(splits) * dsa::kMlaHeads * (dsa::kMlaDv + 1) : 0;
 }
 
 }  // namespace
@@ -485,4 +503,49 @@ const char* dsa_status_string(dsa_status_t status) {
 
 const char* dsa_indexer_last_cuda_error(void) { return g_last_cuda_error; }
 
+size_t dsa_sparse_mla_workspace_size(int32_t batch, int32_t k) {
+    if (batch < 1 || batch > DSA_MAX_BATCH || k < 1 || k > DSA_MLA_MAX_TOPK) return 0;
+    return dsa::kWorkspaceHeaderBytes + mla_partial_floats(batch, mla_splits(batch, k)) * sizeof(float);
+}
+dsa_status_t dsa_sparse_mla_decode(const void* q, const void* kv_cache, int64_t num_pages,
+                                   const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                                   int64_t max_context, const int32_t* topk_idx, int32_t k, float sm_scale,
+                                   float* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    dsa_status_t st = check_shape(batch, max_context);
+    if (st != DSA_OK) return st;
+    if (!q || !kv_cache || !page_table || !seq_lens || !topk_idx || !out || !lse) return DSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(page_table, 4) || !aligned(seq_lens, 4) ||
+        !aligned(topk_idx, 4) || !aligned(out, 16) || !aligned(lse, 16))
+        return DSA_ERR_INVALID_ARG;
+    if (num_pages < 1 || num_pages > kMaxPages) return DSA_ERR_INVALID_ARG;
+    if (k < 1 || k > DSA_MLA_MAX_TOPK || !std::isfinite(sm_scale))
+        return DSA_ERR_INVALID_ARG;
+    const int splits = mla_splits(batch, k);
+    st = check_workspace(workspace, workspace_bytes,
+                         dsa::kWorkspaceHeaderBytes + mla_partial_floats(batch, splits) * sizeof(float));
+    if (st != DSA_OK) return st;
+    CUtensorMap q_map;
+    st = make_rows_map(&q_map, q, int64_t(batch) * DSA_MLA_HEADS, DSA_MLA_DIM, 64, "mla q");
+    if (st != DSA_OK) return st;
+    dsa::MlaParams p{};
+    p.kv = static_cast<const uint8_t*>(kv_cache);
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.topk = topk_idx;
+    p.out = out;
+    p.lse = lse;
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kWorkspaceHeaderBytes);
+    p.o_part = splits > 1 ? part : nullptr;
+    p.lse_part = splits > 1 ? part + size_t(batch) * splits * dsa::kMlaHeads * dsa::kMlaDv : nullptr;
+    p.err = static_cast<uint32_t*>(workspace);
+    p.num_pages = num_pages;
+    p.max_context = max_context;
+    p.table_width = int32_t(max_context / DSA_PAGE_TOKENS);
+    p.batch = batch;
+    p.k = k;
+    p.splits = splits;
+    p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+    const cudaError_t e = dsa::launch_mla(q_map, p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "sparse MLA decode launch");
+}
 }  // extern "C"

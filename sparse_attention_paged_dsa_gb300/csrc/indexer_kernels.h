@@ -84,4 +84,34 @@ int proj_batch_pad(int batch);
 cudaError_t launch_proj(const CUtensorMap& wq_map, const CUtensorMap& ww_map, const CUtensorMap& x_map,
                         const ProjParams& p, cudaStream_t stream);
 
+// Sparse multi-head latent attention decode over the top-k entries: 64 heads,
+// 576-wide bf16 cache entries paged like the index keys, value = first 512 dims.
+constexpr int kMlaHeads = 64;
+constexpr int kMlaDim = 576;
+constexpr int kMlaDv = 512;
+constexpr int kMlaMaxTopk = 2048;
+constexpr int kMlaMaxSplits = 32;
+struct MlaParams {
+    const uint8_t* kv;         // [num_pages, 64, 576] bf16
+    const int32_t* page_table; // [batch, table_width]
+    const int32_t* seq_lens;   // [batch] tokens
+    const int32_t* topk;       // [batch, k] C4 positions, -1 = unused
+    float* out;                // [batch, 64, 512]
+    float* lse;                // [batch, 64]
+    float* o_part;             // [batch, splits, 64, 512] (splits > 1)
+    float* lse_part;           // [batch, splits, 64]
+    uint32_t* err;             // device error word
+    int64_t num_pages;
+    int64_t max_context;
+    int32_t table_width;
+    int32_t batch;
+    int32_t k;
+    int32_t splits;            // CTAs per request, 1..32
+    float sm_scale_log2;       // sm_scale * log2(e)
+};
+size_t mla_smem_bytes();
+// Decode kernel (grid splits x batch) and, for splits > 1, the log-sum-exp merge.
+// q_map: q [batch * 64, 576] bf16, 128-byte-swizzled boxes of 64 x 64.
+cudaError_t launch_mla(const CUtensorMap& q_map, const MlaParams& p, cudaStream_t stream);
+
 }  // namespace dsa

@@ -280,6 +280,70 @@ def with_next_n(case: IndexerCase, next_n: int, dist: str = "normal") -> Indexer
                                w=np.ascontiguousarray(w))
 
 
+# Sparse multi-head latent attention over the selected entries: 64 heads, 576-wide
+# cache entries (512 value + 64 rotary dims), paged like the index keys.
+MLA_HEADS = 64
+MLA_DIM = 576
+MLA_DV = 512
+
+
+@dataclasses.dataclass
+class MlaCase:
+    """Inputs of one sparse-MLA decode call.
+
+    q          uint16 [B, 64, 576]   bf16 bits of the attention query
+    kv         uint16 [P, 64, 576]   bf16 bits of the paged cache (page, entry, dim)
+    page_table int32 [B, W]          the indexer case's table
+    seq_lens   int32 [B]             tokens per request
+    topk       int32 [B, k]          C4 positions, -1 = unused
+    sm_scale   float                 softmax scale
+    """
+
+    name: str
+    q: np.ndarray
+    kv: np.ndarray
+    page_table: np.ndarray
+    seq_lens: np.ndarray
+    max_context: int
+    topk: np.ndarray
+    sm_scale: float
+
+    @property
+    def batch(self) -> int:
+        return int(self.q.shape[0])
+
+
+def random_topk(case: IndexerCase, k: int, seed: int) -> np.ndarray:
+    """Rows shaped like the indexer's top-k output: min(k, live) distinct live positions per
+    request drawn uniformly (stream [seed, 4]), ascending, then -1 padding."""
+    rng = np.random.default_rng([seed, 4])
+    live = case.live_positions()
+    out = np.full((case.batch, k), -1, dtype=np.int32)
+    for b in range(case.batch):
+        n = int(min(k, live[b]))
+        if n:
+            out[b, :n] = np.sort(rng.choice(int(live[b]), size=n, replace=False)).astype(np.int32)
+    return out
+
+
+def mla_case(case: IndexerCase, topk=None, *, k: int = None, sm_scale: float = MLA_DIM ** -0.5) -> MlaCase:
+    """Sparse-MLA inputs on an indexer case's page table and lengths: q and the cache
+    ~ N(0, 1) rounded to bf16 (stream [seed, 3]), one cache page per index-key page.
+    topk: given rows (e.g. the indexer's output) or random_topk(case, k or case.k)."""
+    rng = np.random.default_rng([case.seed, 3])
+    q = _normal_bf16(rng, (case.batch, MLA_HEADS, MLA_DIM))
+    kv = np.empty((case.num_pages, PAGE_ENTRIES, MLA_DIM), dtype=np.uint16)
+    step = 1024
+    for p0 in range(0, case.num_pages, step):  # in chunks: large pools stay within host memory
+        p1 = min(case.num_pages, p0 + step)
+        kv[p0:p1] = _normal_bf16(rng, (p1 - p0, PAGE_ENTRIES, MLA_DIM))
+    if topk is None:
+        topk = random_topk(case, k if k is not None else case.k, case.seed)
+    return MlaCase(name=case.name + "_mla", q=q, kv=kv, page_table=case.page_table, seq_lens=case.seq_lens,
+                   max_context=case.max_context, topk=np.ascontiguousarray(np.asarray(topk, dtype=np.int32)),
+                   sm_scale=float(sm_scale))
+
+
 # The five workloads of the decode indexer, named by what they are.
 WORKLOADS = ("b1_ctx8k_seq512", "b16_ctx8k_mixed", "b64_ctx128k_loguniform",
              "b64_ctx1m_seq512", "b64_ctx128k_dense")
