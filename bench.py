@@ -65,6 +65,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-mtp", action="store_true", help="skip the multi-token (next_n = 2, 4) measurement")
     ap.add_argument("--no-proj", action="store_true", help="skip the q/w projection measurement")
     ap.add_argument("--proj-d-model", type=int, default=7168, help="model width of the synthetic projection")
+    ap.add_argument("--no-mla", action="store_true", help="skip the sparse-MLA decode measurement")
+    ap.add_argument("--literal-pool", action="store_true",
+                    help="dense workload on its literal 8192-page pool (each page in four rows): a small device "
+                         "footprint for profiler captures, not for reported numbers")
     ap.add_argument("--l2-flush", action="store_true",
                     help="memset a 512 MiB buffer before every timed launch (default: back-to-back steps; "
                          "the live keys are twice the L2)")
@@ -408,6 +412,61 @@ def run_proj(args, binding, device, batch):
             "weights": "synthetic N(0, 1/d) bf16: w_q [2048, d], w_w [32, d]; x N(0,1) bf16"}
 
 
+def run_mla(args, case, binding, device, topk, step):
+    """Sparse-MLA decode (64 heads, 576-wide entries) over the indexer's own top-k rows of the
+    workload, on a synthetic cache with one 64-entry page per index-key page; also the indexer
+    step and the attention chained in one graph."""
+    import torch
+    g = torch.Generator(device=device).manual_seed(4343)
+    heads, dim, dv = binding.MLA_HEADS, binding.MLA_DIM, binding.MLA_DV
+    q = torch.randn((case.batch, heads, dim), generator=g, device=device).to(torch.bfloat16)
+    kv = torch.empty((case.num_pages, 64, dim), dtype=torch.bfloat16, device=device)
+    for p0 in range(0, case.num_pages, 4096):  # N(0, 1) in slices (bounded temporary memory)
+        p1 = min(case.num_pages, p0 + 4096)
+        kv[p0:p1] = torch.randn((p1 - p0, 64, dim), generator=g, device=device).to(torch.bfloat16)
+    table = torch.from_numpy(case.page_table).to(device)
+    seq = torch.from_numpy(case.seq_lens).to(device)
+    out = torch.empty((case.batch, heads, dv), dtype=torch.float32, device=device)
+    lse = torch.empty((case.batch, heads), dtype=torch.float32, device=device)
+    ws = torch.zeros(binding.sparse_mla_workspace_size(case.batch, case.k), dtype=torch.uint8, device=device)
+    scale = dim ** -0.5
+    step()  # the indexer's top-k rows of this workload
+    torch.cuda.synchronize(device)
+    used = int((topk >= 0).sum().item())
+
+    def attn():
+        binding.dsa_sparse_mla_decode(q, kv, table, seq, case.max_context, topk, scale, out=out, lse=lse,
+                                      workspace=ws)
+
+    def chained():
+        step()
+        attn()
+
+    for _ in range(max(3, args.warmup)):
+        attn()
+    torch.cuda.synchronize(device)
+    t = graph_us_per_call(attn) * 1e-6
+    t_chain = graph_us_per_call(chained) * 1e-6
+    if binding.get_error(ws) != 0:
+        raise RuntimeError("device error word set in the sparse-MLA run")
+    splits = max(1, min(32, (case.k + 63) // 64, torch.cuda.get_device_properties(device).multi_processor_count
+                        // case.batch))
+    algo = used * dim * 2 + q.numel() * 2 + out.numel() * 4 + lse.numel() * 4
+    peak, peak_kind = measured_hbm_peak()
+    achieved = algo / t / 1e9
+    return {"value": case.batch / t, "unit": "requests/s", "us_per_call": 1e6 * t,
+            "entries_per_s": used / t, "used_entries": used, "splits_per_request": splits,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "kernel": "mla_decode_kernel + mla_merge_kernel",
+                         "peak_kind": f"{peak_kind} (HBM copy bandwidth)", "algorithmic_bytes_per_launch": algo,
+                         "bytes": "used entries x 1152 B + q + o + lse (split partials not counted)"},
+            "indexer_plus_mla_us": 1e6 * t_chain,
+            "timing": "CUDA-graph replay, 20 calls per graph, median of 20",
+            "inputs": "64 heads, 576-dim bf16 q and cache ~ N(0,1) (torch generator on the device), "
+                      "one cache page per index-key page; top-k rows from this workload's indexer step; "
+                      "sm_scale 576^-1/2"}
+
+
 def workload_config(case, world, l2_flush=False):
     live = int(case.live_positions().sum())
     return {"workload": case.name, "batch": case.batch, "max_context": case.max_context,
@@ -471,7 +530,7 @@ def run_ours(args):
 
     from sparse_attention_paged_dsa_gb300 import binding, inputs
     binding.load()
-    case = inputs.workload(args.workload)
+    case = inputs.workload(args.workload, literal_pool=args.literal_pool)
     B, M, K = case.batch, case.max_context // 4, case.k
     live = int(case.live_positions().sum())
 
@@ -539,6 +598,7 @@ def run_ours(args):
     mtp = (run_mtp(args, case, binding, inputs, device, stream, live, pool, table, seq)
            if not args.no_mtp else None)
     proj = run_proj(args, binding, device, case.batch) if not args.no_proj else None
+    mla = run_mla(args, case, binding, device, topk, step) if not args.no_mla else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -576,6 +636,7 @@ def run_ours(args):
         "fp8_key_cache": fp8,
         "multi_token": mtp,
         "qw_projection": proj,
+        "sparse_mla_decode": mla,
         "e2e": e2e,
         "gpu_launches": 2 * n * world,
         "step": "dsa_indexer_fused with the full-width scores row (scores kernel, then top-k kernel)",

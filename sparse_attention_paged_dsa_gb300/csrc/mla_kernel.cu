@@ -13,24 +13,32 @@
 // One CTA per (split, request), one CTA per SM (all of shared memory and
 // TMEM).  The request's non-empty 64-entry blocks of the top-k row are divided
 // into `splits` contiguous ranges; a CTA streams its blocks:
-//   * warps 0 and 2 (even / odd blocks): gather the block's 64 entries with
-//     16-byte cp.async into nine 128-byte-swizzled slabs of 64 rows x 64 dims
-//     (a ring of 8 slab pairs for the 512 value dims, 2 slabs for the rotary
-//     64); unused entries are zero-filled.  Warp 0 also loads q once by TMA.
+//   * warps 0, 2, 3: gather every block's 64 entries with 16-byte cp.async
+//     into nine 128-byte-swizzled slabs of 64 rows x 64 dims (a ring of 8 slab
+//     pairs for the 512 value dims, 2 slabs for the rotary 64); each warp
+//     copies a third of every slab's rows; unused entries are zero-filled.
+//     Warp 0 also loads q once by TMA.
 //   * warp 1: tcgen05.mma kind::f16 --
-//       MMA1  S[head, entry] = Q . K^T, M = 128 (64 heads; the other 64 rows
-//             are ignored), N = 64 entries, K = 576 (36 instructions);
+//       MMA1  S[head, entry] = Q . K^T, M = 64 heads, N = 64 entries, K = 576
+//             (36 instructions; TMEM rows 16 q + i in lanes 32 q + i, i < 16);
 //       MMA2  O^T[dim, head] += V^T . P^T, M = 128 dims x 4, N = 64 heads,
-//             K = 64 entries, V read in place as an MN-major operand.
-//   * warps 4-7: softmax.  Thread h of warps 4-5 holds head h's 64 scores in
-//     registers: block max, exp2, row sum, P row (bf16) to shared memory.  The
+//             K = 64 entries, V read in place as an MN-major operand; the four
+//             accumulators' instructions interleaved.
+//   * warps 4-7: softmax.  Lanes 0-15 of each hold one head's 64 scores in
+//     registers: block max, 2^x, row sum, P row (bf16) to shared memory.  The
 //     running max is raised only when a block exceeds it by more than 2^8; then
 //     all four warps rescale O^T in TMEM (tcgen05.ld / st) before MMA2.  At the
-//     end they normalise O^T and write o (or the split's partial) and lse.
+//     end they normalise O^T into the drained value ring and store o (or the
+//     split's partial) with bulk copies, and write lse.
 // MMA1(n+1) is issued after MMA2(n), so one S accumulator and one P buffer
 // suffice and each completion barrier orders everything before it.  Every wait
 // is bounded (about 1 s); a timeout sets an error bit, the roles drain, and
 // TMEM is freed.
+//
+// What bounds it: a gathered row is 9 separate 128-byte segments, and 16-byte
+// cp.async moves at most about 40 GB/s per SM on this part, with a loaded
+// latency of about 4 us; a 2-block ring (all the shared memory beside q) holds
+// one block in flight while the previous one is computed.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -56,6 +64,8 @@ constexpr int kOffV = kOffP + kSlabBytes;
 constexpr int kOffR = kOffV + kVRing * kPairBytes;
 constexpr int kOffCtl = kOffR + kRRing * kSlabBytes;
 constexpr int kThreadsM = 256;
+constexpr int kProducers = 3;    // warps 0, 2, 3: each copies row groups k = p, p + 3, ... of every slab
+constexpr int kRowGroups = 16;   // 4 rows x 128 bytes per warp-wide cp.async
 constexpr uint32_t kTmemColsM = 512;
 constexpr uint32_t kColS = 0;    // S: 64 columns
 constexpr uint32_t kColO = 128;  // O^T: 4 x 64 columns
@@ -76,6 +86,7 @@ struct __align__(8) MlaCtl {
 };
 constexpr int kSmemM = 1024 + kOffCtl + int(sizeof(MlaCtl));
 static_assert(kSmemM <= 232448, "fits one CTA per SM");
+static_assert(kVRing * kPairBytes == kMlaHeads * kMlaDv * 4, "o fits the value ring");
 
 __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t addr, uint32_t mn_stride) {
     // MN-major, 128-byte swizzle: atoms of 8 K-rows x 64 MN elements (1024 B); atoms
@@ -101,6 +112,20 @@ __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[
         : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 2^x by the hardware's approximate base-2 exponential (flushes subnormal results to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Bulk copy of `bytes` (multiple of 16) from shared to global memory, tracked by this
+// thread's bulk-async group.
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+                 : "memory");
+}
 
 // 16-byte copy global -> shared through L2; src_bytes 0 writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -146,11 +171,11 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kVRing; ++i) {
-            mbar_init(&ctl.v_full[i], 32);  // one noinc arrival per producer lane
+            mbar_init(&ctl.v_full[i], 32 * kProducers);  // one noinc arrival per producer lane
             mbar_init(&ctl.v_empty[i], 1);
         }
         for (int i = 0; i < kRRing; ++i) {
-            mbar_init(&ctl.r_full[i], 32);
+            mbar_init(&ctl.r_full[i], 32 * kProducers);
             mbar_init(&ctl.r_empty[i], 1);
         }
         mbar_init(&ctl.q_full, 1);
@@ -209,9 +234,9 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     float* lse_dst = p.splits == 1 ? p.lse + int64_t(b) * kMlaHeads
                                    : p.lse_part + (int64_t(b) * p.splits + split) * kMlaHeads;
 
-    if (warp == 0 || warp == 2) {
+    if (warp == 0 || warp == 2 || warp == 3) {
         // ================= producers: gather the blocks' entries =================
-        const int pw = warp == 0 ? 0 : 1;
+        const int pw = warp == 0 ? 0 : warp - 1;
         const uint8_t* kv = p.kv;
         bool stop = false;
         if (warp == 0 && lane == 0 && nblk > 0) {
@@ -222,7 +247,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         }
         const int c = lane & 7;  // 16-byte chunk of a 128-byte slab row
 #pragma unroll 1
-        for (int n = pw; n < nblk && !stop; n += 2) {
+        for (int n = 0; n < nblk && !stop; ++n) {
             const int blk = ctl.blocks[n];
             // byte offsets of entries lane and lane + 32 (-1: unused, zero-filled)
             int64_t off[2];
@@ -238,13 +263,15 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                         atomicOr(p.err, kErrBadPage);
                 }
             }
-            // this lane copies chunk c of rows r = 4 i + lane / 8, i = 0..15
-            int64_t row_off[16];
+            // this lane copies chunk c of rows r = 4 k + lane / 8 for its row groups k = pw + 3 i
+            constexpr int kMaxGroups = (kRowGroups + kProducers - 1) / kProducers;
+            int64_t row_off[kMaxGroups];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int r = 4 * i + (lane >> 3);
-                const int64_t v = i < 8 ? off[0] : off[1];
-                row_off[i] = __shfl_sync(0xffffffffu, v, r & 31);
+            for (int i = 0; i < kMaxGroups; ++i) {
+                const int k = pw + kProducers * i;
+                const int r = 4 * k + (lane >> 3);
+                const int64_t v = k < 8 ? off[0] : off[1];
+                row_off[i] = __shfl_sync(0xffffffffu, v, r & 31);  // k is warp-uniform
             }
 #pragma unroll 1
             for (int j = 0; j <= 4; ++j) {  // value pairs 0..3, then the rotary slab
@@ -278,8 +305,10 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                     const int s = slab0 + hs;
                     const uint32_t slab = dst_base + hs * kSlabBytes;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int r = 4 * i + (lane >> 3);
+                    for (int i = 0; i < kMaxGroups; ++i) {
+                        const int k = pw + kProducers * i;
+                        if (k >= kRowGroups) break;
+                        const int r = 4 * k + (lane >> 3);
                         const uint32_t dst = slab + r * 128 + ((c ^ (r & 7)) << 4);
                         const bool use_row = row_off[i] >= 0;
                         const uint8_t* src = use_row ? kv + row_off[i] + s * 128 + c * 16 : kv;
@@ -304,7 +333,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            constexpr uint32_t kIdesc1 = idesc_bf16_f32(128, 64);
+            constexpr uint32_t kIdesc1 = idesc_bf16_f32(64, 64);  // S: 64 heads x 64 entries
             constexpr uint32_t kIdesc2 = idesc_bf16_f32(128, 64) | (1u << 15);  // A (V^T) MN-major
             const uint32_t q_addr = s_base + kOffQ;
             const uint32_t p_addr = s_base + kOffP;
@@ -357,15 +386,16 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                 }
                 tc_fence_after_sync();
                 const uint64_t bp = smem_desc_kmajor_sw128(p_addr);
-#pragma unroll 1
-                for (int j = 0; j < 4; ++j) {  // MMA2: dims [128 j, 128 j + 128)
-                    const uint32_t vbase = s_base + kOffV + vslot[j] * kPairBytes;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ss(tmem_base + kColO + 64u * j, desc_mn_sw128(vbase + kk * 2048, kSlabBytes),
+                for (int kk = 0; kk < 4; ++kk) {  // MMA2: dims [128 j, 128 j + 128), the four interleaved
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        umma_bf16_ss(tmem_base + kColO + 64u * j,
+                                     desc_mn_sw128(s_base + kOffV + vslot[j] * kPairBytes + kk * 2048, kSlabBytes),
                                      bp + 2u * kk, kIdesc2, (n > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&ctl.v_empty[vslot[j]]);
                 }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) umma_commit(&ctl.v_empty[vslot[j]]);
             }
             if (stop) {
                 atomicOr(p.err, kErrWaitTimeout);
@@ -377,8 +407,10 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     } else if (warp >= 4) {
         // ================= softmax and output: warps 4..7 =================
         const int quad = warp & 3;
-        const bool head_thr = quad < 2;
-        const int h = quad * 32 + lane;
+        // MMA1 (M = 64) leaves head 16 q + i in TMEM lane 32 q + i, i < 16: lanes 0..15 of each
+        // softmax warp own one head each
+        const bool head_thr = lane < 16;
+        const int h = quad * 16 + (lane & 15);
         const uint32_t lane_addr = tmem_base + (uint32_t(quad * 32) << 16);
         const float c2 = p.sm_scale_log2;
         float m_used = -INFINITY, l_sum = 0.f;
@@ -397,7 +429,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
             tc_fence_after_sync();
             float x[kBlk];
             float m_blk = -INFINITY;
-            if (head_thr) {
+            {   // whole warp: tcgen05.ld is warp-collective; lanes 16..31 read unused lanes
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(lane_addr + kColS, r);
                 tmem_ld_wait(r);
@@ -408,6 +440,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     x[32 + i] = ((u_hi >> i) & 1u) ? __uint_as_float(r[i]) * c2 : -INFINITY;
+            }
+            if (head_thr) {
 #pragma unroll
                 for (int i = 0; i < kBlk; ++i) m_blk = fmaxf(m_blk, x[i]);
                 if (n == 0) m_used = m_blk;
@@ -443,8 +477,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                     uint32_t packed[4];
 #pragma unroll
                     for (int q2 = 0; q2 < 4; ++q2) {
-                        const float p0 = exp2f(x[8 * ch + 2 * q2] - m_used);
-                        const float p1 = exp2f(x[8 * ch + 2 * q2 + 1] - m_used);
+                        const float p0 = ex2_approx(x[8 * ch + 2 * q2] - m_used);
+                        const float p1 = ex2_approx(x[8 * ch + 2 * q2 + 1] - m_used);
                         const __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
                         const float2 back = __bfloat1622float2(v);
                         l_sum += back.x + back.y;
@@ -476,6 +510,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                 lse_dst[h] = (m_used + log2f(l_sum)) * kLn2;
             }
             softmax_bar_sync();
+            // o [64 heads, 512 dims] fp32 staged in the drained value ring, then bulk stores
+            float* o_s = reinterpret_cast<float*>(tiles + kOffV);
 #pragma unroll 1
             for (int j = 0; j < 8; ++j) {
                 uint32_t r[32];
@@ -484,7 +520,16 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                 const int d = (j >> 1) * 128 + quad * 32 + lane;
                 const int h0 = (j & 1) * 32;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o_dst[(h0 + i) * kMlaDv + d] = __uint_as_float(r[i]) * ctl.inv_l[h0 + i];
+                for (int i = 0; i < 32; ++i) o_s[(h0 + i) * kMlaDv + d] = __uint_as_float(r[i]) * ctl.inv_l[h0 + i];
+            }
+            fence_proxy_async_smem();
+            softmax_bar_sync();
+            if (threadIdx.x == 128) {
+                for (int c = 0; c < 4; ++c)
+                    bulk_store(o_dst + c * (kMlaHeads * kMlaDv / 4), s_base + kOffV + c * (kMlaHeads * kMlaDv),
+                               uint32_t(kMlaHeads * kMlaDv));
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
             }
         }
     }
