@@ -213,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // Both walk the same unit sequence (page ids fetched one batch ahead).  Per own unit:
         // lane 0 posts the metadata and issues the two code boxes; all 32 lanes copy the
         // unit's scales (cp.async, arriving on the stage's full barrier).  A row change is
-        // numbered in sequence order; the warp owning the unit where the row starts stages
-        // the row's query and head weights for the splitter.
+        // numbered in sequence order; warp 0 stages every row's query and head weights for the
+        // splitter, in that order, so that its waits on a raw-query slot are one phase apart.
         const int me = warp == 0 ? 0 : 1;
         const uint64_t pol_keys = l2_policy_evict_first();
         const uint64_t pol_q = l2_policy_evict_last();
@@ -239,16 +239,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     ++nrows;
                     prev_b = bi;
                 }
-                if ((seq & 1) != me) continue;  // the other producer's unit
-                const int pi = __shfl_sync(0xffffffffu, cur.pair, i);
-                const int g0 = __shfl_sync(0xffffffffu, cur.pg0, i);
-                const int g1 = __shfl_sync(0xffffffffu, cur.pg1, i);
-                const bool ok0 = g0 >= 0 && g0 < p.num_pages;
-                const bool ok1 = g1 >= 0 && g1 < p.num_pages;
-                const int stage = seq % kStages;
                 int failed = 0;
-                if (lane == 0) {
-                    if (new_row) {  // stage the request's query and head weights for the splitter
+                if (new_row && me == 0) {  // stage the request's query and head weights for the splitter
+                    if (lane == 0) {
                         const int k = nrows - 1, qs = k % kQRaw;
                         if (!mbar_wait(&ctl.qraw_empty[qs], ((k / kQRaw) & 1) ^ 1u, &ctl.abort)) {
                             failed = 1;
@@ -264,7 +257,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                             q_mine[kQRaw - 1] = k;
                         }
                     }
-                    if (!failed && !mbar_wait(&ctl.empty[stage], (uint32_t(seq / kStages) & 1u) ^ 1u, &ctl.abort))
+                    if (__shfl_sync(0xffffffffu, failed, 0)) {
+                        stop = true;
+                        break;
+                    }
+                }
+                if ((seq & 1) != me) continue;  // the other producer's unit
+                const int pi = __shfl_sync(0xffffffffu, cur.pair, i);
+                const int g0 = __shfl_sync(0xffffffffu, cur.pg0, i);
+                const int g1 = __shfl_sync(0xffffffffu, cur.pg1, i);
+                const bool ok0 = g0 >= 0 && g0 < p.num_pages;
+                const bool ok1 = g1 >= 0 && g1 < p.num_pages;
+                const int stage = seq % kStages;
+                if (lane == 0) {
+                    if (!mbar_wait(&ctl.empty[stage], (uint32_t(seq / kStages) & 1u) ^ 1u, &ctl.abort))
                         failed = 1;
                     if (!failed) {
                         if (!ok0 || (g1 != -2 && !ok1)) atomicOr(p.err, kErrBadPage);
@@ -298,19 +304,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             cur_cnt = nxt_cnt;
             cur = nxt;
         }
-        // End-of-work markers, posted by the warp that owns the end place: one for the splitter
-        // (row-change number nrows), one for the MMA issuer and epilogue (unit number seq).
-        if (!stop && (seq & 1) == me) {
-            const int stage = seq % kStages;
+        // End-of-work markers: the splitter's (row-change number nrows) from warp 0, which
+        // stages every query; the MMA issuer's and epilogue's (unit number seq) from the warp
+        // that owns that place.
+        if (!stop && me == 0) {
             int failed = 0;
             if (lane == 0) {
                 const int qs = nrows % kQRaw;
-                if (!mbar_wait(&ctl.qraw_empty[qs], ((nrows / kQRaw) & 1) ^ 1u, &ctl.abort) ||
-                    !mbar_wait(&ctl.empty[stage], (uint32_t(seq / kStages) & 1u) ^ 1u, &ctl.abort)) {
+                if (!mbar_wait(&ctl.qraw_empty[qs], ((nrows / kQRaw) & 1) ^ 1u, &ctl.abort)) {
                     failed = 1;
                 } else {
                     ctl.qrow[qs] = -1;
                     mbar_arrive(&ctl.qraw_full[qs]);
+                }
+            }
+            if (__shfl_sync(0xffffffffu, failed, 0)) stop = true;
+        }
+        if (!stop && (seq & 1) == me) {
+            const int stage = seq % kStages;
+            int failed = 0;
+            if (lane == 0) {
+                if (!mbar_wait(&ctl.empty[stage], (uint32_t(seq / kStages) & 1u) ^ 1u, &ctl.abort)) {
+                    failed = 1;
+                } else {
                     ctl.meta[seq % kRing] = kEndOfWork;
                     mbar_arrive(&ctl.full[stage]);
                 }

@@ -175,8 +175,9 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
     if (warp == 0 || warp == 2) {
         // ================= producers: warp 0 issues the CTA's even units, warp 2 the odd ones =================
         // Both walk the same unit sequence (page ids fetched one batch ahead); a row change is
-        // numbered in sequence order and its query tile is loaded by the warp that owns the
-        // unit where the row starts.
+        // numbered in sequence order and warp 0 loads every row's query tile, in that order, so
+        // that its waits on a query slot are one phase apart (a slot's next load waits for the
+        // release of the load before it, which it issued itself).
         const int me = warp >> 1;
         const uint64_t pol_keys = l2_policy_evict_first();
         const uint64_t pol_q = l2_policy_evict_last();
@@ -201,13 +202,9 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
                     ++nrows;
                     prev_b = bi;
                 }
-                if ((seq & 1) != me) continue;  // the other producer's unit
-                const int pi = __shfl_sync(0xffffffffu, cur.pair, i);
-                const int g0 = __shfl_sync(0xffffffffu, cur.pg0, i);
-                const int g1 = __shfl_sync(0xffffffffu, cur.pg1, i);
                 int failed = 0;
-                if (lane == 0) {
-                    if (new_row) {  // this request's query tile goes to the row's q slot
+                if (new_row && me == 0) {  // this request's query tile goes to the row's q slot
+                    if (lane == 0) {
                         const int k = nrows - 1, qs = k % kQSlots;
                         if (!mbar_wait(&ctl.qempty[qs], ((k / kQSlots) & 1) ^ 1u, &ctl.abort)) {
                             failed = 1;
@@ -220,9 +217,19 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
                             q_mine[kQSlots - 1] = k;
                         }
                     }
+                    if (__shfl_sync(0xffffffffu, failed, 0)) {
+                        stop = true;
+                        break;
+                    }
+                }
+                if ((seq & 1) != me) continue;  // the other producer's unit
+                const int pi = __shfl_sync(0xffffffffu, cur.pair, i);
+                const int g0 = __shfl_sync(0xffffffffu, cur.pg0, i);
+                const int g1 = __shfl_sync(0xffffffffu, cur.pg1, i);
+                if (lane == 0) {
                     const int stage = seq % kStages;
                     const uint32_t phase = uint32_t(seq / kStages) & 1u;
-                    if (!failed && !mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort)) failed = 1;
+                    if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl.abort)) failed = 1;
                     if (!failed) {
                         const bool ok0 = g0 >= 0 && g0 < p.num_pages;
                         const bool ok1 = g1 >= 0 && g1 < p.num_pages;

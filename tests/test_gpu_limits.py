@@ -79,3 +79,43 @@ def test_past_the_limits_rejected(gpu_lib):
     assert lib.dsa_indexer_workspace_size(1025, 1024, 1) == 0
     torch.cuda.synchronize()
     assert int(buf.count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("path", ["bf16", "fp8", "two_token"])
+def test_short_mixed_rows_query_slots(gpu_lib, oracle, path):
+    """1024 requests of one to three two-page units in a mixed order, so that consecutive rows
+    start on units of either producer warp and the two query slots turn over every few units;
+    repeated five times, each run must leave the error word clear and match the oracle."""
+    import torch
+    rng = np.random.default_rng(4049)
+    seqs = rng.choice(np.array([1, 512, 513, 1024, 1025, 1536]), size=1024)
+    case = I.make_case(name="shortrows", batch=1024, max_context=2048, seq_lens=seqs, num_pages=4096, k=64,
+                       seed=41)
+    q, w, pool, table, seq = gpu_lib.to_device(case)
+    ws = gpu_lib.new_workspace(case.batch, case.max_context, case.k)
+    if path == "fp8":
+        f = I.with_fp8_keys(case)
+        codes, scales = gpu_lib.to_device_fp8(f)
+        ref = oracle.case_scores_fp8(f)
+        run = lambda: gpu_lib.dsa_indexer_scores_fp8(q, w, codes, scales, table, seq, case.max_context, workspace=ws)
+    elif path == "two_token":
+        m = I.with_next_n(case, 2)
+        qm = torch.from_numpy(m.q.view("int16")).cuda().view(torch.bfloat16)
+        wm = torch.from_numpy(m.w).cuda()
+        ref = oracle.case_scores_mtp(m).reshape(-1, case.max_context // 4)
+        run = lambda: gpu_lib.dsa_indexer_scores_mtp(qm, wm, pool, table, seq, case.max_context,
+                                                     workspace=ws).reshape(-1, case.max_context // 4)
+    else:
+        ref = oracle.case_scores(case)
+        run = lambda: gpu_lib.dsa_indexer_scores(q, w, pool, table, seq, case.max_context, workspace=ws)
+    live = np.isfinite(ref)
+    for _ in range(5):
+        s = run()
+        torch.cuda.synchronize()
+        assert gpu_lib.get_error(ws) == 0
+        s = s.cpu().numpy()
+        assert np.array_equal(np.isfinite(s), live)
+        for r in range(ref.shape[0]):
+            if live[r].any():
+                rel = np.abs(s[r][live[r]] - ref[r][live[r]]).max() / np.abs(ref[r][live[r]]).max()
+                assert rel <= 3e-3, f"row {r}: {rel}"
