@@ -73,7 +73,7 @@ template <int Q>
 struct Cfg {
     static constexpr int kCtasPerSm = Q == 1 ? 3 : 2;
     static constexpr int kStages = Q == 1 ? 3 : 4;           // 16 KiB stages per CTA, shared by the producers
-    static constexpr int kEpiGroups = 1;                      // epilogue groups of 4 warps
+    static constexpr int kEpiGroups = Q >= 3 ? 2 : 1;         // epilogue groups of 4 warps (Q >= 3: Q passes per unit)
     static constexpr int kQSlots = 2;
     static constexpr int kAccStages = Q <= 2 ? 4 : 2;
     static constexpr int kMetaRing = 16;                      // >= kStages + kAccStages + 1
@@ -104,7 +104,7 @@ struct __align__(16) SmemCtl {
     uint32_t tmem_base;
     int abort;
     int32_t meta[Cfg<Q>::kMetaRing];
-    __align__(16) float wtok[4][Q > 1 ? Q : 1][kHeads];  // Q > 1: each epilogue warp's copy of the request's head weights
+    __align__(16) float wtok[4 * Cfg<Q>::kEpiGroups][Q > 1 ? Q : 1][kHeads];  // Q > 1: each epilogue warp's copy of the head weights
     RowTable rows;
 };
 
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
                 } else {  // this warp's copy of the Q x 32 head weights; per-token causal lengths
                     __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < Q; ++j) ctl.wtok[quad][j][lane] = __ldg(p.w + (int64_t(b) * Q + j) * kHeads + lane);
+                    for (int j = 0; j < Q; ++j) ctl.wtok[warp - 4][j][lane] = __ldg(p.w + (int64_t(b) * Q + j) * kHeads + lane);
                     __syncwarp();
                     int64_t L = p.seq_lens[b];
                     L = L < 0 ? 0 : (L > p.max_context ? p.max_context : L);
@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
                         tc_fence_before_sync();
                         mbar_arrive(&ctl.tempty[acc]);
                     }
-                    const float4* wr = reinterpret_cast<const float4*>(ctl.wtok[quad][j]);
+                    const float4* wr = reinterpret_cast<const float4*>(ctl.wtok[warp - 4][j]);
                     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
                     for (int h4 = 0; h4 < kHeads / 4; ++h4) {
