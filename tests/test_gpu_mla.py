@@ -144,3 +144,14 @@ def test_mla_host_checks(gpu_lib):
     with pytest.raises(b.DsaError):
         b.dsa_sparse_mla_decode(q, kv, table, seq, mc.max_context, topk, 0.1, workspace=ws)
     assert b.sparse_mla_workspace_size(1, 0) == 0 and b.sparse_mla_workspace_size(1, 2049) == 0
+
+
+def test_mla_more_requests_than_sms(gpu_lib, oracle):
+    """200 requests (more than the SMs: one split each, no merge, several waves of CTAs),
+    k = 1000 (a ragged last block), lengths 1..4096 tokens; every request checked."""
+    rng = np.random.default_rng(91)
+    seqs = rng.integers(1, 4097, size=200)
+    case = I.make_case(name="many", batch=200, max_context=4096, seq_lens=seqs, num_pages=3400, k=1000, seed=92)
+    mc = I.mla_case(case)
+    o, lse = _run(gpu_lib, mc)
+    _check(o, lse, mc, oracle)
