@@ -58,7 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-sample-rows", type=int, default=32,
                     help="rows of the workload the CPU baseline times (about 10-30 s on one core)")
-    ap.add_argument("--reference-rows-per-step", type=int, default=2)
+    ap.add_argument("--reference-rows-per-step", type=int, default=1,
+                    help="rows of the workload the reference arm (the oracle) scores per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context-scaling", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the fp8 key-cache measurement")
