@@ -9,7 +9,8 @@ lse: the row sum of rounded weights is within 2^-9 relatively, so |lse - lse_ref
 1e-5 |lse|.  Cases: one block; many requests with ragged top-k rows split across CTAs and
 merged; holes, duplicates, positions past the live length and empty rows; the running-max
 rescale (late blocks dominate); the indexer's own top-k rows on a mixed-length workload; the
-full 64-request, 128K-context workload sampled; determinism; host argument checks."""
+full 64-request, 128K-context workload sampled; more requests than SMs and the maximum batch
+(one split each, several waves); a zero scale (the plain mean); determinism; host argument checks."""
 import numpy as np
 import pytest
 
@@ -155,3 +156,24 @@ def test_mla_more_requests_than_sms(gpu_lib, oracle):
     mc = I.mla_case(case)
     o, lse = _run(gpu_lib, mc)
     _check(o, lse, mc, oracle)
+
+
+def test_mla_max_batch(gpu_lib, oracle):
+    """1024 requests (the boundary's maximum), k = 64, lengths 1..2048 tokens: about seven waves of
+    CTAs, one split each; every request checked."""
+    rng = np.random.default_rng(93)
+    seqs = rng.integers(1, 2049, size=1024)
+    case = I.make_case(name="maxb", batch=1024, max_context=2048, seq_lens=seqs, num_pages=8192, k=64, seed=94)
+    mc = I.mla_case(case)
+    o, lse = _run(gpu_lib, mc)
+    _check(o, lse, mc, oracle)
+
+
+def test_mla_zero_scale_is_the_mean(gpu_lib, oracle):
+    """sm_scale = 0: every used entry has weight 1/n, so o is the plain mean of the used value rows
+    and lse = log n (checked against the oracle, which computes the same softmax)."""
+    mc = I.mla_case(I.workload("b16_ctx8k_mixed"), sm_scale=0.0)
+    o, lse = _run(gpu_lib, mc)
+    _check(o, lse, mc, oracle)
+    n = (mc.topk >= 0).sum(axis=1)
+    np.testing.assert_allclose(lse[:, 0], np.log(n), rtol=1e-5)
