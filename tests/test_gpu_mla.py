@@ -177,3 +177,23 @@ def test_mla_zero_scale_is_the_mean(gpu_lib, oracle):
     _check(o, lse, mc, oracle)
     n = (mc.topk >= 0).sum(axis=1)
     np.testing.assert_allclose(lse[:, 0], np.log(n), rtol=1e-5)
+
+
+def test_mla_workspace_reused(gpu_lib, oracle):
+    """Three calls on one workspace, on two different inputs: each result equals a call on a fresh
+    workspace (nothing a call leaves in the workspace changes the next one)."""
+    import torch
+    b = gpu_lib
+    mc1 = I.mla_case(I.workload("b16_ctx8k_mixed"))
+    mc2 = I.mla_case(I.workload("b16_ctx8k_mixed"), sm_scale=0.02)
+    ws = torch.zeros(b.sparse_mla_workspace_size(mc1.batch, mc1.topk.shape[1]), dtype=torch.uint8, device="cuda")
+    outs = []
+    for mc in (mc1, mc2, mc1):
+        q, kv, table, seq, topk = _dev(mc)
+        o, lse = b.dsa_sparse_mla_decode(q, kv, table, seq, mc.max_context, topk, mc.sm_scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert b.get_error(ws, clear=False) == 0
+        outs.append((o.cpu().numpy(), lse.cpu().numpy()))
+    for (o, lse), mc in zip(outs, (mc1, mc2, mc1)):
+        of, lf = _run(b, mc)
+        assert np.array_equal(o, of) and np.array_equal(lse, lf)
