@@ -6,8 +6,29 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <mutex>
 
 namespace dsa {
+
+constexpr int kMaxDevices = 64;
+
+// A kernel's dynamic shared-memory limit, set once per device.  Safe when
+// several host threads make their first calls at the same time (call_once
+// per device); every later call returns the first call's result.  One
+// static instance per kernel, used on the launching thread's current device.
+struct SmemLimitOnce {
+    std::once_flag flag[kMaxDevices];
+    cudaError_t result[kMaxDevices] = {};
+
+    template <typename Kernel>
+    cudaError_t apply(int dev, Kernel* kernel, int bytes) {
+        if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        std::call_once(flag[dev], [&] {
+            result[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        });
+        return result[dev];
+    }
+};
 
 // Fixed problem geometry.
 constexpr int kHeads = 32;

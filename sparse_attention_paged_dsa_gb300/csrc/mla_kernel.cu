@@ -591,16 +591,12 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(const MlaParams p) {
 size_t mla_smem_bytes() { return size_t(kSmemM); }
 
 cudaError_t launch_mla(const CUtensorMap& q_map, const MlaParams& p, cudaStream_t stream) {
-    static bool configured[64] = {};
+    static SmemLimitOnce smem_limit;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemM);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+    e = smem_limit.apply(dev, mla_decode_kernel, kSmemM);
+    if (e != cudaSuccess) return e;
     if (p.splits < 1 || p.splits > kMlaMaxSplits) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -283,17 +283,13 @@ __global__ void __launch_bounds__(kThreadsP, kCtasPerSmP)
 template <int kBp>
 cudaError_t launch_proj_bp(const CUtensorMap& wq_map, const CUtensorMap& ww_map, const CUtensorMap& x_map,
                            const ProjParams& p, cudaStream_t stream) {
-    static bool configured[64] = {};
+    static SmemLimitOnce smem_limit;
     const size_t smem = 1024 + size_t(stages_for(kBp)) * stage_bytes(kBp) + sizeof(ProjCtl);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(proj_kernel<kBp>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+    e = smem_limit.apply(dev, proj_kernel<kBp>, int(smem));
+    if (e != cudaSuccess) return e;
     if (p.k_split < 1 || p.k_split > kMaxSplitP) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -547,16 +547,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 cudaError_t launch_scores_fp8(const CUtensorMap& codes_map, const CUtensorMap& qraw_map, const CUtensorMap& w_map,
                               const ScoresParams& p, cudaStream_t stream) {
-    static bool configured[64] = {};
+    static SmemLimitOnce smem_limit;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(scores_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+    e = smem_limit.apply(dev, scores_fp8_kernel, int(kSmemBytes));
+    if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;

@@ -466,17 +466,12 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
 template <int Q>
 cudaError_t launch_scores_q(const CUtensorMap& keys_map, const CUtensorMap& q_map, const ScoresParams& p,
                             cudaStream_t stream) {
-    static bool configured[64] = {};
+    static SmemLimitOnce smem_limit;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(scores_kernel<Q>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(Layout<Q>::kSmemBytes));
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+    e = smem_limit.apply(dev, scores_kernel<Q>, int(Layout<Q>::kSmemBytes));
+    if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;

@@ -41,8 +41,12 @@ constexpr int kKeysPerThread = 32;                  // register path: keys per t
 constexpr int kRegCap = kThreads * kKeysPerThread;  // 32768
 constexpr int kLoadsPerThread = kRegCap / 4 / kThreads;  // float4 loads per thread on the register path
 
+// Order-preserving 32-bit key of an fp32 score: a > b as floats iff
+// key(a) > key(b).  -0 is first mapped to +0, because the two are equal in
+// fp32 order and equal scores must tie (and then go to the lower position).
 __device__ __forceinline__ uint32_t order_key(float x) {
-    const uint32_t u = __float_as_uint(x);
+    uint32_t u = __float_as_uint(x);
+    u = u == 0x80000000u ? 0u : u;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
@@ -600,17 +604,12 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
     const int64_t want = p.row_width + p.row_width / 32 + 1;
     const int cache_cap = p.row_width > p.k ? int(want < kCacheCap ? want : kCacheCap) : 0;
     const size_t smem = size_t(cache_cap) * sizeof(uint32_t);
-    static bool configured[64] = {};
+    static SmemLimitOnce smem_limit;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(kCacheCap * sizeof(uint32_t)));
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+    e = smem_limit.apply(dev, topk_kernel, int(kCacheCap * sizeof(uint32_t)));
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(p.batch) * unsigned(p.tokens));
     cfg.blockDim = dim3(kThreads);

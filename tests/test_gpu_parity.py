@@ -198,3 +198,58 @@ def test_topk_rows_that_defeat_the_sample(gpu_lib, oracle):
     for i, n in enumerate(n_live):
         ref = oracle.topk_row(rows[i].astype(np.float64), n, k)
         np.testing.assert_array_equal(got[i], ref, err_msg=f"row {i}")
+
+
+def _signed_zero_rows(rng, M):
+    """Rows whose k-th largest score is 0 and that hold both +0 and -0 (equal in fp32 order,
+    so they tie and go to the lower position whatever their sign)."""
+    rows, n_live = [], []
+    zeros = np.sort(rng.choice(M, 3000, replace=False))    # more zeros than k: k cuts the zero band
+    for first in (-0.0, 0.0):                               # both sign orders along the positions
+        r = -np.abs(rng.standard_normal(M)).astype(np.float32) - 0.5
+        if first == 0.0:
+            signs = np.where(np.arange(zeros.size) % 2 == 0, np.float32(0.0), np.float32(-0.0))
+        else:
+            signs = np.where(np.arange(zeros.size) % 2 == 0, np.float32(-0.0), np.float32(0.0))
+        r[zeros] = signs
+        rows.append(r); n_live.append(M)
+    r = np.where(rng.random(M) < 0.5, np.float32(-0.0), np.float32(0.0)).astype(np.float32)
+    rows.append(r); n_live.append(M)                        # every score a signed zero
+    r = -np.abs(rng.standard_normal(M)).astype(np.float32) - 0.5
+    r[zeros[:1500]] = np.float32(-0.0)
+    r[zeros[1500:]] = np.float32(0.0)                       # every -0 before every +0
+    r[:40] = 3.0
+    rows.append(r); n_live.append(M)
+    return np.stack(rows), n_live
+
+
+def test_topk_signed_zeros_tie(gpu_lib, oracle):
+    """+0 and -0 are equal scores: the top-k takes the lower positions among them, as the oracle
+    (which ranks in fp64, where -0 == +0) does, through the single-token and multi-token entry points."""
+    import torch
+    rng = np.random.default_rng(1234)
+    M, k = 32768, 2048
+    rows, n_live = _signed_zero_rows(rng, M)
+    assert np.signbit(rows[0][rows[0] == 0]).any() and (~np.signbit(rows[0][rows[0] == 0])).any()
+    got = _topk_on_rows(gpu_lib, rows, n_live, k)
+    for i, n in enumerate(n_live):
+        ref = oracle.topk_row(rows[i].astype(np.float64), n, k)
+        np.testing.assert_array_equal(got[i], ref, err_msg=f"row {i}")
+    # a short row (k < n <= 256: ranked by direct comparison) of mixed zeros
+    short = np.full((1, 256), -1.0, np.float32)
+    short[0, :200] = np.where(rng.random(200) < 0.5, np.float32(-0.0), np.float32(0.0))
+    short[0, 7] = 1.0
+    got = _topk_on_rows(gpu_lib, short, [230], 50)
+    np.testing.assert_array_equal(got[0], oracle.topk_row(short[0].astype(np.float64), 230, 50))
+    # the same rows through the multi-token entry point: two tokens per request, token j of
+    # request b is row 2b + j (both tokens see the whole row: seq_len = 4M gives n = M for both)
+    B2 = (rows.shape[0] + 1) // 2
+    pad = np.concatenate([rows, rows[:1]]) if rows.shape[0] % 2 else rows
+    s = torch.from_numpy(np.ascontiguousarray(pad.reshape(B2, 2, M), dtype=np.float32)).cuda()
+    seq = torch.full((B2,), 4 * M, dtype=torch.int32, device="cuda")
+    t = gpu_lib.dsa_indexer_topk_mtp(s, seq, 4 * M, k)
+    torch.cuda.synchronize()
+    t = t.cpu().numpy().reshape(-1, k)
+    for i in range(rows.shape[0]):
+        ref = oracle.topk_row(pad[i].astype(np.float64), M, k)
+        np.testing.assert_array_equal(t[i], ref, err_msg=f"multi-token row {i}")
