@@ -58,12 +58,12 @@
  *     max_context is treated as max_context and a negative one as 0; a live
  *     page id outside [0, num_pages) is not read and its positions score -inf.
  *     Each case sets a bit in the workspace error word (DSA_DEVERR_*).
- *   - Workspace: a caller-owned device buffer of at least
- *     dsa_indexer_workspace_size() bytes, zeroed once before first use
- *     (dsa_indexer_workspace_init or any memset to 0).  Its first 256 bytes
- *     hold the sticky device error word; the rest of them is reserved and
- *     stays zero.  Calls that share a workspace must be ordered on one
- *     stream.
+ *   - Workspace: a caller-owned device buffer, 256-byte aligned, of at least
+ *     dsa_indexer_workspace_size() bytes (every entry point accepts that
+ *     size), zeroed once before first use (dsa_indexer_workspace_init or any
+ *     memset to 0).  Its first 256 bytes hold the sticky device error word;
+ *     the rest of them is reserved and stays zero.  Calls that share a
+ *     workspace must be ordered on one stream.
  */
 #ifndef DSA_INDEXER_H
 #define DSA_INDEXER_H
@@ -124,9 +124,9 @@ DSA_API dsa_status_t dsa_indexer_scores(const void *q, const float *w, const voi
 
 /*
  * Step 4 on a scores row: topk_idx [batch, k] = the min(k, n_b) positions
- * t < n_b with the largest scores[b, t] (fp32 order; equal scores: lower t
- * first), in ascending t, then -1.  Reads only scores[b, t] for t < n_b, and
- * none when n_b <= k.  1 <= k <= max_context / 4.
+ * t < n_b with the largest scores[b, t] (fp32 order, -0 == +0; equal scores:
+ * lower t first), in ascending t, then -1.  Reads only scores[b, t] for
+ * t < n_b, and none when n_b <= k.  1 <= k <= max_context / 4.
  */
 DSA_API dsa_status_t dsa_indexer_topk(const float *scores, const int32_t *seq_lens, int32_t batch,
                               int64_t max_context, int32_t k, int32_t *topk_idx,
@@ -137,6 +137,8 @@ DSA_API dsa_status_t dsa_indexer_topk(const float *scores, const int32_t *seq_le
  * by dsa_indexer_scores and topk_idx equals dsa_indexer_topk on it.  With
  * scores_opt == NULL nothing of size max_context is written: live scores go to
  * the workspace and the cost is O(live positions) plus O(batch x k).
+ * The two kernels run back to back on `stream`; the top-k kernel is the one
+ * dsa_indexer_topk launches.
  */
 DSA_API dsa_status_t dsa_indexer_fused(const void *q, const float *w, const void *key_pool,
                                int64_t num_pages, const int32_t *page_table,
@@ -154,18 +156,28 @@ DSA_API dsa_status_t dsa_indexer_fused(const void *q, const float *w, const void
  *
  * Scratch: a library-owned device array of 256 B + 16 MiB, held by every GPU
  * that loads the library until the process exits.  batch x max_context / 4
- * fp32 live-score slots must fit in the 16 MiB, otherwise the call returns
- * DSA_ERR_UNSUPPORTED and launches nothing.  The first call on a device looks
- * up the array's device address (once per device) and must come before any
- * stream capture on that device.  All calls share the array: calls that
- * overlap on the GPU (unordered streams) race on it.  Each call clears the
- * array's error word before it launches; device error bits are not reported
- * by this entry point.  Same inputs and output as dsa_indexer_fused.
+ * fp32 live-score slots must fit in the 16 MiB (e.g. 64 requests at 256K
+ * tokens, 128 at 128K), otherwise the call returns
+ * DSA_ERR_UNSUPPORTED and launches nothing.  Arguments are checked exactly as
+ * by dsa_indexer_fused, before the scratch is touched.  The first call on a
+ * device looks up the array's device address (once per device) and must come
+ * before any stream capture on that device.  All calls share the array: calls
+ * that overlap on the GPU (unordered streams) race on it.  The array's device
+ * error word is sticky like a workspace's; read it with
+ * dsa_indexer_noalloc_get_error.  Same inputs and output as dsa_indexer_fused.
  */
 DSA_API dsa_status_t dsa_indexer_fused_noalloc(const void *q, const float *w, const void *key_pool,
                                        int64_t num_pages, const int32_t *page_table,
                                        const int32_t *seq_lens, int32_t batch, int64_t max_context,
                                        int32_t k, int32_t *topk_idx, void *stream);
+
+/*
+ * dsa_indexer_get_error on the current device's scratch array of
+ * dsa_indexer_fused_noalloc (DSA_DEVERR_* bits of every noalloc call since the
+ * last clear).  Synchronises `stream`; allocates nothing.  No counterpart on
+ * the source pages either.
+ */
+DSA_API dsa_status_t dsa_indexer_noalloc_get_error(uint32_t *code, int clear, void *stream);
 
 /*
  * fp8 key cache.  The deployment on the pages keeps its KV cache in fp8
@@ -215,7 +227,9 @@ DSA_API dsa_status_t dsa_indexer_fused_fp8(const void *q, const float *w, const 
  */
 #define DSA_MAX_NEXT_N 4
 
-/* Workspace bytes for the multi-token entry points (0 for an invalid shape). */
+/* Workspace bytes for the multi-token entry points (0 for an invalid shape):
+ * 256 bytes of header plus, for dsa_indexer_fused_mtp without a scores row,
+ * batch x next_n x max_context / 4 fp32 live-score slots. */
 DSA_API size_t dsa_indexer_workspace_size_mtp(int32_t batch, int32_t next_n, int64_t max_context, int32_t k);
 
 /* dsa_indexer_scores for next_n tokens per request. */

@@ -11,6 +11,7 @@
 #include <cstring>
 
 #include "../../include/dsa_indexer.h"
+#include "api_checks.h"
 #include "indexer_kernels.h"
 
 namespace {
@@ -246,6 +247,17 @@ dsa_status_t run_topk(const float* scores, const int32_t* seq_lens, int32_t batc
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "top-k kernel launch");
 }
 
+// Workspace of a fused call over `nrows` score rows: the header, plus the
+// live-score slots when no scores row is given.
+size_t fused_workspace_bytes(int64_t nrows, int64_t max_context, bool with_slots) {
+    return dsa::kWorkspaceHeaderBytes + (with_slots ? size_t(nrows) * size_t(max_context / 4) * sizeof(float) : 0);
+}
+
+float* fused_rows(void* workspace, float* scores_opt) {
+    return scores_opt ? scores_opt
+                      : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kWorkspaceHeaderBytes);
+}
+
 // Splits of a request's top-k row across CTAs (one CTA per SM): enough to fill
 // the current device once, at most one per 64-entry block and kMlaMaxSplits.
 int mla_splits(int32_t batch, int32_t k) {
@@ -265,12 +277,29 @@ size_t mla_partial_floats(int32_t batch, int splits) {
 
 }  // namespace
 
+namespace dsa {
+
+dsa_status_t check_fused_args(const void* q, const float* w, const void* key_pool, int64_t num_pages,
+                              const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                              int64_t max_context, int32_t k, const int32_t* topk_idx, const float* scores_opt) {
+    dsa_status_t st = check_shape(batch, max_context);
+    if (st != DSA_OK) return st;
+    st = check_score_inputs(q, w, key_pool, num_pages, page_table, seq_lens);
+    if (st != DSA_OK) return st;
+    if (!topk_idx || !aligned(topk_idx, 4)) return DSA_ERR_INVALID_ARG;
+    if (scores_opt && !aligned(scores_opt, 16)) return DSA_ERR_INVALID_ARG;
+    if (k < 1 || int64_t(k) > max_context / 4) return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+}
+
+}  // namespace dsa
+
 extern "C" {
 
 size_t dsa_indexer_workspace_size(int32_t batch, int64_t max_context, int32_t k) {
     (void)k;
     if (check_shape(batch, max_context) != DSA_OK) return 0;
-    return dsa::kWorkspaceHeaderBytes + size_t(batch) * size_t(max_context / 4) * sizeof(float);
+    return fused_workspace_bytes(batch, max_context, true);
 }
 
 dsa_status_t dsa_indexer_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -312,19 +341,13 @@ dsa_status_t dsa_indexer_fused(const void* q, const float* w, const void* key_po
                                const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
                                int64_t max_context, int32_t k, int32_t* topk_idx, float* scores_opt,
                                void* workspace, size_t workspace_bytes, void* stream) {
-    dsa_status_t st = check_shape(batch, max_context);
+    dsa_status_t st = dsa::check_fused_args(q, w, key_pool, num_pages, page_table, seq_lens, batch, max_context, k,
+                                            topk_idx, scores_opt);
     if (st != DSA_OK) return st;
-    st = check_score_inputs(q, w, key_pool, num_pages, page_table, seq_lens);
-    if (st != DSA_OK) return st;
-    if (!topk_idx || !aligned(topk_idx, 4)) return DSA_ERR_INVALID_ARG;
-    if (scores_opt && !aligned(scores_opt, 16)) return DSA_ERR_INVALID_ARG;
-    if (k < 1 || int64_t(k) > max_context / 4) return DSA_ERR_INVALID_ARG;
-    const size_t need = scores_opt ? dsa::kWorkspaceHeaderBytes : dsa_indexer_workspace_size(batch, max_context, k);
-    st = check_workspace(workspace, workspace_bytes, need);
+    st = check_workspace(workspace, workspace_bytes, fused_workspace_bytes(batch, max_context, !scores_opt));
     if (st != DSA_OK) return st;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    float* rows = scores_opt ? scores_opt
-                             : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kWorkspaceHeaderBytes);
+    float* rows = fused_rows(workspace, scores_opt);
     st = run_scores(q, w, key_pool, num_pages, page_table, seq_lens, batch, max_context, rows, scores_opt ? 1 : 0,
                     workspace, s);
     if (st != DSA_OK) return st;
@@ -359,12 +382,10 @@ dsa_status_t dsa_indexer_fused_fp8(const void* q, const float* w, const void* ke
     if (!topk_idx || !aligned(topk_idx, 4)) return DSA_ERR_INVALID_ARG;
     if (scores_opt && !aligned(scores_opt, 16)) return DSA_ERR_INVALID_ARG;
     if (k < 1 || int64_t(k) > max_context / 4) return DSA_ERR_INVALID_ARG;
-    const size_t need = scores_opt ? dsa::kWorkspaceHeaderBytes : dsa_indexer_workspace_size(batch, max_context, k);
-    st = check_workspace(workspace, workspace_bytes, need);
+    st = check_workspace(workspace, workspace_bytes, fused_workspace_bytes(batch, max_context, !scores_opt));
     if (st != DSA_OK) return st;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    float* rows = scores_opt ? scores_opt
-                             : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kWorkspaceHeaderBytes);
+    float* rows = fused_rows(workspace, scores_opt);
     st = run_scores_fp8(q, w, key_codes, key_scales, num_pages, page_table, seq_lens, batch, max_context, rows,
                         scores_opt ? 1 : 0, workspace, s);
     if (st != DSA_OK) return st;
@@ -374,7 +395,7 @@ dsa_status_t dsa_indexer_fused_fp8(const void* q, const float* w, const void* ke
 size_t dsa_indexer_workspace_size_mtp(int32_t batch, int32_t next_n, int64_t max_context, int32_t k) {
     (void)k;
     if (check_shape(batch, max_context) != DSA_OK || next_n < 1 || next_n > DSA_MAX_NEXT_N) return 0;
-    return dsa::kWorkspaceHeaderBytes + size_t(batch) * size_t(next_n) * size_t(max_context / 4) * sizeof(float);
+    return fused_workspace_bytes(int64_t(batch) * next_n, max_context, true);
 }
 
 dsa_status_t dsa_indexer_scores_mtp(const void* q, const float* w, const void* key_pool, int64_t num_pages,
@@ -420,13 +441,11 @@ dsa_status_t dsa_indexer_fused_mtp(const void* q, const float* w, const void* ke
     if (!topk_idx || !aligned(topk_idx, 4)) return DSA_ERR_INVALID_ARG;
     if (scores_opt && !aligned(scores_opt, 16)) return DSA_ERR_INVALID_ARG;
     if (k < 1 || int64_t(k) > max_context / 4) return DSA_ERR_INVALID_ARG;
-    const size_t need =
-        scores_opt ? dsa::kWorkspaceHeaderBytes : dsa_indexer_workspace_size_mtp(batch, next_n, max_context, k);
-    st = check_workspace(workspace, workspace_bytes, need);
+    st = check_workspace(workspace, workspace_bytes,
+                         fused_workspace_bytes(int64_t(batch) * next_n, max_context, !scores_opt));
     if (st != DSA_OK) return st;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    float* rows = scores_opt ? scores_opt
-                             : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dsa::kWorkspaceHeaderBytes);
+    float* rows = fused_rows(workspace, scores_opt);
     st = run_scores(q, w, key_pool, num_pages, page_table, seq_lens, batch, max_context, rows, scores_opt ? 1 : 0,
                     workspace, s, next_n);
     if (st != DSA_OK) return st;

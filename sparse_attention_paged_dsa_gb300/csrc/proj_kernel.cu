@@ -49,28 +49,6 @@ constexpr int kThreadsP = 192;               // producer, MMA, 4 epilogue warps
 constexpr int kCtasPerSmP = 2;
 constexpr int kMaxSplitP = 8;                // portable cluster size
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// All threads of all CTAs of the cluster; orders shared-memory writes before remote reads.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Shared-memory address of the same variable in CTA `cta` of the cluster.  Volatile (like the
-// load below) so that neither moves above the cluster barrier that orders the writes before it.
-__device__ __forceinline__ uint32_t cluster_addr(const void* local_ptr, uint32_t cta) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(cta));
-    return remote;
-}
-// Load from distributed shared memory; callers issue all of a sum's loads before its adds.
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
-}
 
 struct __align__(8) ProjCtl {
     uint64_t full[8];

@@ -82,6 +82,33 @@ __device__ __forceinline__ void pdl_wait_prior_grid() { asm volatile("griddepcon
 // Allow the next programmatic-dependent launch in the stream to be scheduled.
 __device__ __forceinline__ void pdl_allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster; orders shared-memory writes before remote reads.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory address of the same variable in CTA `cta` of the cluster.  Volatile (like the
+// loads below) so that neither moves above the cluster barrier that orders the writes before it.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local_ptr, uint32_t cta) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(cta));
+    return remote;
+}
+
+// Loads from distributed shared memory.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
 // ---------------------------------------------------------------- L2 hints
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;

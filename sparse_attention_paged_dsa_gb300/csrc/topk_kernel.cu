@@ -29,6 +29,7 @@
 #include <cstdint>
 
 #include "indexer_kernels.h"
+#include "order_key.cuh"
 #include "sm103_ptx.cuh"
 
 namespace dsa {
@@ -40,15 +41,6 @@ constexpr int kCacheCap = 49152;                    // keys held in shared memor
 constexpr int kKeysPerThread = 32;                  // register path: keys per thread
 constexpr int kRegCap = kThreads * kKeysPerThread;  // 32768
 constexpr int kLoadsPerThread = kRegCap / 4 / kThreads;  // float4 loads per thread on the register path
-
-// Order-preserving 32-bit key of an fp32 score: a > b as floats iff
-// key(a) > key(b).  -0 is first mapped to +0, because the two are equal in
-// fp32 order and equal scores must tie (and then go to the lower position).
-__device__ __forceinline__ uint32_t order_key(float x) {
-    uint32_t u = __float_as_uint(x);
-    u = u == 0x80000000u ? 0u : u;
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 struct TopkSmem {
     uint32_t hist[2048];

@@ -68,11 +68,12 @@ def test_host_argument_checks_launch_nothing(gpu_lib):
     assert fused_call(k=257) == b.DSA_ERR_INVALID_ARG      # k > max_context / 4
     assert fused_call(out=None) == b.DSA_ERR_INVALID_ARG
     assert fused_call(wsb=1024) == b.DSA_ERR_WORKSPACE     # no row: needs the live-score area
+    assert fused_call(rows=P(scores.data_ptr()), wsb=255) == b.DSA_ERR_WORKSPACE  # a row: the header only
     torch.cuda.synchronize()
     # nothing was launched by the rejected calls
     assert torch.equal(scores, sentinel)
     assert lib.dsa_indexer_workspace_size(2, 1000, 16) == 0
-    assert lib.dsa_indexer_workspace_size(2, 1024, 16) == 256 + 2 * 256 * 4
+    assert lib.dsa_indexer_workspace_size(2, 1024, 16) == nbytes == 256 + 2 * 256 * 4
     assert lib.dsa_status_string(b.DSA_ERR_WORKSPACE).decode().startswith("workspace")
 
 
