@@ -58,10 +58,11 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-sample-rows", type=int, default=32,
                     help="rows of the workload the CPU baseline times (about 10-30 s on one core)")
-    ap.add_argument("--reference-rows-per-step", type=int, default=1,
-                    help="rows of the workload the reference arm (the oracle) scores per step")
+    ap.add_argument("--reference-rows-per-step", type=int, default=0,
+                    help="rows of the workload the reference arm (the oracle) scores per step (0: one per host core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context-scaling", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table (all five workloads)")
     ap.add_argument("--no-fp8", action="store_true", help="skip the fp8 key-cache measurement")
     ap.add_argument("--no-mtp", action="store_true", help="skip the multi-token (next_n = 2, 4) measurement")
     ap.add_argument("--no-proj", action="store_true", help="skip the q/w projection measurement")
@@ -191,22 +192,50 @@ def profiled_traffic(summary, src):
         return None
 
 
-def cpu_baseline(case, rows: int):
-    """The fp64 oracle as it stands, single-threaded, on `rows` rows of the workload."""
+def host_cores():
+    """Host cores this process may run on (read at run time)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rows(case, rows, threads):
+    """The oracle as it stands (scores, then the full-sort top-k) on the given rows of a workload,
+    one row per call, `threads` calls at a time.  The oracle keeps no state and ctypes releases the
+    GIL during each call, so the calls run on `threads` host cores.  Returns (live positions, s)."""
+    import concurrent.futures as cf
     from oracle import oracle
-    oracle.build()
-    rows = max(1, min(rows, case.batch))
     from sparse_attention_paged_dsa_gb300.inputs import IndexerCase
-    sub = IndexerCase("sample", case.q[:rows], case.w[:rows], case.key_pool, case.page_table[:rows],
-                      case.seq_lens[:rows], case.max_context, case.k)
+    oracle.build()
+
+    def one(b):
+        sub = IndexerCase("row", case.q[b:b + 1], case.w[b:b + 1], case.key_pool, case.page_table[b:b + 1],
+                          case.seq_lens[b:b + 1], case.max_context, case.k)
+        oracle.case_topk(sub, oracle.case_scores(sub))
+        return int(sub.live_positions().sum())
+
     t0 = time.perf_counter()
-    s = oracle.case_scores(sub)
-    oracle.case_topk(sub, s)
-    dt = time.perf_counter() - t0
-    pos = int(sub.live_positions().sum())
-    return {"value": pos / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {rows} of {case.batch} rows ({pos} live positions), fp64 scores + full-sort top-k, "
-                      f"{dt:.2f} s"}
+    if threads <= 1:
+        pos = sum(one(b) for b in rows)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            pos = sum(ex.map(one, rows))
+    return pos, time.perf_counter() - t0
+
+
+def cpu_baseline(case, rows: int):
+    """The fp64 oracle as it stands on the host's cores: all of them (one row per core at a time) on
+    every row of the workload, and one core on the first `rows` rows."""
+    cores = host_cores()
+    pos_all, dt_all = oracle_rows(case, list(range(case.batch)), cores)
+    rows = max(1, min(rows, case.batch))
+    pos_one, dt_one = oracle_rows(case, list(range(rows)), 1)
+    return {"value": pos_all / dt_all, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"all {case.batch} rows ({pos_all} live positions), fp64 scores + full-sort top-k, "
+                      f"one row per call on {cores} threads, {dt_all:.2f} s",
+            "single_core": {"value": pos_one / dt_one, "unit": UNIT, "cores": 1, "kind": "oracle",
+                            "sample": f"first {rows} rows ({pos_one} live positions), {dt_one:.2f} s"}}
 
 
 def evict_l2(buf):
@@ -306,6 +335,85 @@ def context_scaling(binding, inputs, device):
             "workload": "64 requests x 512 tokens, k=2048, same keys and page ids; CUDA-graph replay"}
 
 
+CONFIG_WORKLOADS = ["b1_ctx8k_seq512", "b16_ctx8k_mixed", "b64_ctx128k_loguniform", "b64_ctx1m_seq512",
+                    "b64_ctx128k_dense"]
+
+
+def run_configs(args, binding, inputs, device, stream, main_case, main_dev):
+    """Every named workload through the three call shapes: the fused call with the full-width scores
+    row, the fused call without it (live scores in the workspace), and the scores entry point alone.
+    Each is timed twice: warm (20 calls captured in one CUDA graph, median of 20 replays: back to back,
+    as in a decode loop) and with L2 evicted before every call (a 512 MiB read outside the events,
+    median of 30 isolated calls)."""
+    import torch
+    peak, peak_kind = measured_hbm_peak()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    out = {"timing": "warm: CUDA-graph replay of 20 calls, median of 20; l2_evicted: CUDA events around each of "
+                     "30 calls, a 512 MiB read before each (outside the events), median",
+           "peak_gbs": peak, "peak_kind": f"{peak_kind} (HBM copy bandwidth)"}
+
+    def time_both(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        warm = graph_us_per_call(fn)
+        _, per = time_loop(fn, 30, stream, lambda: evict_l2(flush))
+        return {"warm": warm, "l2_evicted": 1e6 * statistics.median(per)}
+
+    for name in CONFIG_WORKLOADS:
+        case = main_case if name == main_case.name else inputs.workload(name)
+        q, w, pool, table, seq = main_dev if case is main_case else binding.to_device(case, device)
+        B, M, K = case.batch, case.max_context // 4, case.k
+        live = int(case.live_positions().sum())
+        scores = torch.empty((B, M), dtype=torch.float32, device=device)
+        topk = torch.empty((B, K), dtype=torch.int32, device=device)
+        ws = binding.new_workspace(B, case.max_context, K, device)
+        fused_row = time_both(lambda: binding.dsa_indexer_fused(q, w, pool, table, seq, case.max_context, K,
+                                                                topk_idx=topk, scores=scores, workspace=ws))
+        fused_no_row = time_both(lambda: binding.dsa_indexer_fused(q, w, pool, table, seq, case.max_context, K,
+                                                                   topk_idx=topk, workspace=ws))
+        scores_only = time_both(lambda: binding.dsa_indexer_scores(q, w, pool, table, seq, case.max_context,
+                                                                   scores=scores, workspace=ws))
+        if binding.get_error(ws) != 0:
+            raise RuntimeError(f"device error word set in the {name} run")
+        key_bytes = live * KEY_BYTES_PER_POSITION
+        gbs = lambda us: key_bytes / (us * 1e-6) / 1e9
+        entry = {
+            "batch": B, "max_context": case.max_context, "k": K, "live_positions": live, "live_key_bytes": key_bytes,
+            "fused_row_us": fused_row, "fused_no_row_us": fused_no_row, "scores_us": scores_only,
+            "positions_per_s": {t: live / (fused_row[t] * 1e-6) for t in ("warm", "l2_evicted")},
+            "step_gbs": {t: gbs(fused_row[t]) for t in ("warm", "l2_evicted")},
+            "step_frac": {t: gbs(fused_row[t]) / peak for t in ("warm", "l2_evicted")},
+            "scores_kernel_frac": {t: gbs(scores_only[t]) / peak for t in ("warm", "l2_evicted")},
+            "fused_over_scores": {t: fused_row[t] / scores_only[t] for t in ("warm", "l2_evicted")},
+            "scores_row_bytes": B * M * 4,
+        }
+        if name == "b64_ctx1m_seq512":
+            # The scores entry point writes the whole [B, max_context / 4] row: its -inf fill at this
+            # width against the same requests at an 8K width (same keys and page ids).
+            small = inputs.IndexerCase("b64_ctx8k_seq512", case.q, case.w, case.key_pool,
+                                       case.page_table[:, :8192 // inputs.PAGE_TOKENS].copy(), case.seq_lens,
+                                       8192, case.k)
+            q8, w8, pool8, table8, seq8 = binding.to_device(small, device)
+            scores8 = torch.empty((B, 8192 // 4), dtype=torch.float32, device=device)
+            ws8 = binding.new_workspace(B, 8192, K, device)
+            s8 = time_both(lambda: binding.dsa_indexer_scores(q8, w8, pool8, table8, seq8, 8192, scores=scores8,
+                                                              workspace=ws8))
+            entry["scores_api_fill"] = {
+                "width_1m": {"row_bytes": B * M * 4, "us": scores_only,
+                             "row_gbs": {t: B * M * 4 / (scores_only[t] * 1e-6) / 1e9 for t in scores_only}},
+                "width_8k": {"row_bytes": B * 2048 * 4, "us": s8,
+                             "row_gbs": {t: B * 2048 * 4 / (s8[t] * 1e-6) / 1e9 for t in s8}},
+                "ratio_1m_over_8k": {t: scores_only[t] / s8[t] for t in s8},
+                "note": "the scores entry point is O(max_context) by contract (it writes the full-width row); "
+                        "the O(live) bound is the fused call without a row (context_scaling)"}
+            if binding.get_error(ws8) != 0:
+                raise RuntimeError("device error word set in the 8K-width scores run")
+        out[name] = entry
+    del flush
+    return out
+
+
 def run_fp8(args, case, binding, inputs, device, stream, live):
     """The same workload on the fp8 key cache: fused step (events, back-to-back) and scores kernel alone."""
     import torch
@@ -372,7 +480,7 @@ def run_mtp(args, case, binding, inputs, device, stream, live, pool, table, seq)
         B, M, K = c.batch, c.max_context // 4, c.k
         scores = torch.empty((B, Q, M), dtype=torch.float32, device=device)
         topk = torch.empty((B, Q, K), dtype=torch.int32, device=device)
-        ws = torch.zeros(256, dtype=torch.uint8, device=device)
+        ws = torch.zeros(binding.workspace_size_mtp(B, Q, c.max_context, K), dtype=torch.uint8, device=device)
 
         def step():
             binding.dsa_indexer_fused_mtp(q, w, pool, table, seq, c.max_context, K, topk_idx=topk, scores=scores,
@@ -509,19 +617,12 @@ def run_reference(args):
         return 0
     from sparse_attention_paged_dsa_gb300 import inputs
     case = inputs.workload(args.workload)
-    from oracle import oracle
-    oracle.build()
-    from sparse_attention_paged_dsa_gb300.inputs import IndexerCase
-    r = max(1, min(args.reference_rows_per_step, case.batch))
+    cores = host_cores()
+    r = max(1, min(args.reference_rows_per_step or cores, case.batch))
 
-    def step(i):
+    def step(i):  # r rows of the workload, one per host core at a time
         b0 = (i * r) % case.batch
-        idx = [(b0 + j) % case.batch for j in range(r)]
-        sub = IndexerCase("sample", case.q[idx], case.w[idx], case.key_pool, case.page_table[idx],
-                          case.seq_lens[idx], case.max_context, case.k)
-        s = oracle.case_scores(sub)
-        oracle.case_topk(sub, s)
-        return int(sub.live_positions().sum())
+        return oracle_rows(case, [(b0 + j) % case.batch for j in range(r)], min(r, cores))[0]
 
     for i in range(args.warmup):
         step(i)
@@ -533,8 +634,9 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(case, 1), "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{r} rows of {case.batch} per step (fp64 oracle, one host core)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(r, cores), "kind": "oracle",
+                             "sample": f"{r} rows of {case.batch} per step (fp64 oracle, one row per call on "
+                                       f"{min(r, cores)} host threads)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -618,6 +720,8 @@ def run_ours(args):
         e2e = run_e2e(args, case, binding, scores, topk, ws, device, stream, world, live)
 
     scaling_1m = context_scaling(binding, inputs, device) if not args.no_context_scaling else None
+    configs = (run_configs(args, binding, inputs, device, stream, case, (q, w, pool, table, seq))
+               if not args.no_configs else None)
     fp8 = run_fp8(args, case, binding, inputs, device, stream, live) if not args.no_fp8 else None
     mtp = (run_mtp(args, case, binding, inputs, device, stream, live, pool, table, seq)
            if not args.no_mtp else None)
@@ -657,6 +761,7 @@ def run_ours(args):
                    "one CUDA-event pair around the K back-to-back steps"),
         "cpu_baseline": cpu,
         "context_scaling": scaling_1m,
+        "configs": configs,
         "fp8_key_cache": fp8,
         "multi_token": mtp,
         "qw_projection": proj,
