@@ -161,5 +161,52 @@ __device__ __forceinline__ void fill_dead_tails(const RowTable& t, const ScoresP
     }
 }
 
+// The same -inf fill done by one warp per CTA (lane = `lane`), off the
+// epilogue's path: the dead float4s of all rows, taken in row order as one
+// flat range, are split into equal contiguous shares, one per CTA, and each
+// share is written by the warp with consecutive lanes on consecutive float4s.
+__device__ __forceinline__ void fill_dead_tails_warp(const RowTable& t, const ScoresParams& p, int lane,
+                                                     int tokens = 1) {
+    const int64_t M4 = p.row_width / 4;
+    const float neg_inf = __int_as_float(0xff800000);
+    const float4 ninf4 = make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
+    const int batch = p.batch;
+    auto dead4 = [&](int b) {  // dead float4s of each of request b's rows
+        const int64_t e4 = int64_t(t.unit_start[b + 1] - t.unit_start[b]) * (kUnitPositions / 4);
+        return e4 < M4 ? M4 - e4 : int64_t(0);
+    };
+    // Lane l sums the rows [l * per, (l + 1) * per); a warp scan gives each lane's flat start.
+    const int per = (batch + 31) / 32;
+    const int r0 = min(lane * per, batch), r1 = min(r0 + per, batch);
+    int64_t mine = 0;
+    for (int b = r0; b < r1; ++b) mine += dead4(b) * tokens;
+    int64_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    const int64_t total = __shfl_sync(0xffffffffu, incl, 31);  // < 2^31 float4s
+    // This CTA's share [lo, hi): floor(total * c / grid) in double is exact (the product is
+    // below 2^53 and the quotient is at least 1 / grid away from the next integer).
+    const int64_t lo = int64_t(double(total) * blockIdx.x / gridDim.x);
+    const int64_t hi = int64_t(double(total) * (blockIdx.x + 1) / gridDim.x);
+    const int64_t start = incl - mine;
+    uint32_t owners = __ballot_sync(0xffffffffu, mine > 0 && start < hi && start + mine > lo);
+    while (owners) {  // lanes whose rows meet the share, in row order
+        const int src = __ffs(owners) - 1;
+        owners &= owners - 1u;
+        int64_t acc = __shfl_sync(0xffffffffu, start, src);
+        for (int b = min(src * per, batch); b < min(src * per + per, batch) && acc < hi; ++b) {
+            const int64_t d = dead4(b);
+            for (int j = 0; j < tokens; ++j, acc += d) {
+                const int64_t s0 = acc > lo ? acc : lo, s1 = acc + d < hi ? acc + d : hi;
+                float4* row = reinterpret_cast<float4*>(p.out + (int64_t(b) * tokens + j) * p.row_width) + (M4 - d);
+                for (int64_t i = s0 + lane; i < s1; i += 32) __stcs(row + (i - acc), ninf4);
+            }
+        }
+    }
+}
+
 }  // namespace scores
 }  // namespace dsa

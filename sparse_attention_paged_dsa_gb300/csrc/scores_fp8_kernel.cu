@@ -11,21 +11,22 @@
 // The key codes go from HBM to shared memory by TMA and from there straight
 // into tcgen05.mma kind::f8f6f4 (no conversion pass over the keys).  The MMA
 // wants both operands in 8-bit formats, so each bf16 query head is written as
-// an exact sum of two e4m3 terms under a per-head power-of-two scale S_h:
-//     q_h / S_h = hi_h + lo_h / 16,   hi_h = e4m3(q_h / S_h),
-//     lo_h = e4m3(16 * (q_h / S_h - hi_h)),
-// with S_h = 2^(e_h - 7), e_h the binary exponent of max_d |q_h,d|.  A bf16
-// value carries 8 significant bits; hi keeps the top 4 (rounded) and the
-// rounding remainder is a multiple of the value's last bit no larger than
-// 8 of them, which e4m3 holds exactly.  So every element within 2^13 of its
-// head's largest one is represented exactly; smaller ones keep an absolute
-// error below 2^-14 of the head's largest element.  The 32 heads become
-// N = 64 MMA rows (hi and lo of head h at rows 2h and 2h+1), and
-//     q_h . k_t = S_h * scale_t * (acc[2h] + acc[2h+1] / 16)
-// where acc is the fp32 accumulator over the e4m3 codes.  S_h and scale_t
-// are positive, so relu commutes with them: the epilogue forms
-// w_h * S_h * relu(acc[2h] + acc[2h+1] / 16), sums over heads and multiplies
-// by scale_t once.
+// a sum of two e4m3 terms under a per-head power-of-two scale S_h:
+//     q_h / S_h = hi_h + lo_h,   hi_h = e4m3(q_h / S_h),   lo_h = e4m3(q_h / S_h - hi_h),
+// with S_h = 2^(e_h - 7), e_h the binary exponent of max_d |q_h,d| (so the
+// largest element of the head lies in [128, 256)).  A bf16 value carries 8
+// significant bits; hi keeps the top 4 (rounded) and the remainder is at most
+// 8 of the value's last bits, which e4m3 holds exactly down to its smallest
+// quantum 2^-9.  So every element within a factor 2^9 of its head's largest
+// one is represented exactly, and smaller ones keep an absolute error of at
+// most 2^-10 in units of S_h, below 2^-17 of the head's largest element.
+// The two terms are two K-halves of one contraction: four MMAs of K = 32
+// accumulate  acc[h] = sum_d code_t,d * (hi_h,d + lo_h,d)  into one fp32
+// column per head (N = 32), so
+//     q_h . k_t = S_h * scale_t * acc[h].
+// S_h and scale_t are positive, so relu commutes with them: the epilogue
+// forms w_h * S_h * relu(acc[h]), sums over heads and multiplies by scale_t
+// once.
 //
 // Pipeline (per CTA, three CTAs per SM, persistent grid sized by the device):
 //   * warps 0 and 3 (producers): the unit schedule and page ids
@@ -38,14 +39,15 @@
 //     as a whole page, so the small scale rows do not go through TMA).  Per
 //     request change the owner of the first unit stages the bf16 query and
 //     its head weights (TMA) for the splitter.
-//   * warp 2: per request change, splits the query into the hi/lo e4m3 tile
-//     the MMA reads (64-byte swizzle) and w_h * S_h, in a small ring that
-//     the epilogue frees when it leaves the request.
-//   * warp 1: tcgen05.mma kind::f8f6f4, M=128 keys x N=64 x K=32, two per
-//     unit, into one of 4 TMEM accumulators of 64 columns.
-//   * warps 4-7: tcgen05.ld, the hi/lo combination, relu, weighted head sum,
-//     key scale, live mask, 128-byte stores; first the -inf fill of the dead
-//     tail of every row when a full row is requested.
+//   * warp 2: per request change, splits the query into the hi and lo e4m3
+//     tiles the MMA reads (64-byte swizzle) and w_h * S_h, in a small ring
+//     that the epilogue frees when it leaves the request.
+//   * warp 1: tcgen05.mma kind::f8f6f4, M=128 keys x N=32 heads x K=32, four
+//     per unit (hi then lo, two K-slices each), into one of 4 TMEM
+//     accumulators of 32 columns.
+//   * warps 4-7: tcgen05.ld, relu, weighted head sum, key scale, live mask,
+//     128-byte stores; first the -inf fill of the dead tail of every row when
+//     a full row is requested.
 //   * Every wait is bounded (about 1 s); a timeout sets an error bit, stops
 //     all roles, drains in-flight copies and MMAs and frees TMEM.
 #include <cuda.h>
@@ -66,19 +68,20 @@ using namespace scores;
 // Three CTAs per SM, two TMA-issuing producer warps each: one issuing thread
 // keeps too few 4 KiB boxes in flight to cover HBM latency (a TMA instruction
 // takes about 120 cycles to issue), so each SM runs six issuers.
-constexpr int kStages = 4;       // key-code stages of 8 KiB (two pages), shared by the producer warps
+constexpr int kStages = 5;       // key-code stages of 8 KiB (two pages), shared by the producer warps
 constexpr int kQRaw = 2;         // staged bf16 query rows
 constexpr int kQSlots = 2;       // split e4m3 query tiles
-constexpr int kAccStages = 2;
-constexpr int kRing = 8;         // metadata and scale ring, >= kStages + kAccStages + 1
+constexpr int kAccStages = 4;
+constexpr int kRing = 16;        // metadata and scale ring, >= kStages + kAccStages + 1 (a power of two)
 constexpr int kCtasPerSm = 3;
-constexpr int kAccCols = 64;     // N = 2 x 32 heads
+constexpr int kAccCols = 32;     // N = 32 heads
 constexpr uint32_t kTmemCols = kAccStages * kAccCols;  // 128
 constexpr int kConvThreads = 32;
 constexpr int kEpiThreads = 128;
 constexpr int kThreads = 128 + kEpiThreads;                // producers 0 and 3, MMA 1, splitter 2, epilogue 4..7
 constexpr int kStageBytes = 2 * kPageCodeBytes;            // 8 KiB: 128 keys x 64 B
-constexpr int kQ8Bytes = 2 * kHeads * kHeadDim;            // 4 KiB: 64 rows x 64 B
+constexpr int kQHalfBytes = kHeads * kHeadDim;             // 2 KiB: 32 heads x 64 B (hi or lo)
+constexpr int kQ8Bytes = 2 * kQHalfBytes;                  // hi tile, then lo tile
 constexpr int kUnitScaleBytes = 2 * kPageScaleBytes;       // 512 B
 constexpr int kWRowBytes = kHeads * 4;                     // 128 B
 constexpr uint32_t kFullArrivals = 1 + 32;                 // producer lane 0 + its 32 lanes' scale copies
@@ -146,7 +149,7 @@ __device__ __forceinline__ void split8(const float* x, uint2& hi, uint2& lo) {
     for (int i = 0; i < 4; ++i) {
         h[i] = f32x2_to_e4m3x2(x[2 * i], x[2 * i + 1]);
         const float2 hv = e4m3x2_to_f32x2(h[i]);
-        l[i] = f32x2_to_e4m3x2(16.f * (x[2 * i] - hv.x), 16.f * (x[2 * i + 1] - hv.y));
+        l[i] = f32x2_to_e4m3x2(x[2 * i] - hv.x, x[2 * i + 1] - hv.y);
     }
     hi = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
     lo = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
@@ -371,12 +374,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                     tc_fence_after_sync();
                     const uint64_t a_desc = smem_desc_kmajor_sw64(smem_u32(tiles + size_t(stage) * kStageBytes));
-                    const uint64_t b_desc =
-                        smem_desc_kmajor_sw64(smem_u32(q8 + size_t(q_used % kQSlots) * kQ8Bytes));
+                    const uint8_t* qt = q8 + size_t(q_used % kQSlots) * kQ8Bytes;
+                    const uint64_t b_hi = smem_desc_kmajor_sw64(smem_u32(qt));
+                    const uint64_t b_lo = smem_desc_kmajor_sw64(smem_u32(qt + kQHalfBytes));
                     const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
+                    // K = 32 codes per MMA: +32 bytes = +2 in the address field.  hi, then lo,
+                    // against the same two K-slices of the keys, into one accumulator.
 #pragma unroll
-                    for (int kk = 0; kk < kHeadDim / 32; ++kk)  // K = 32 codes per MMA: +32 bytes = +2 in the address field
-                        umma_f8_ss(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, kIdesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < kHeadDim / 32; ++kk)
+                        umma_f8_ss(d_tmem, a_desc + 2u * kk, b_hi + 2u * kk, kIdesc, kk > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < kHeadDim / 32; ++kk)
+                        umma_f8_ss(d_tmem, a_desc + 2u * kk, b_lo + 2u * kk, kIdesc, 1u);
                     umma_commit(&ctl.empty[stage]);
                     umma_commit(&ctl.tfull[acc]);
                 }
@@ -449,9 +458,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 uint2 hi0, lo0, hi1, lo1;
                 split8(x, hi0, lo0);
                 split8(x + 8, hi1, lo1);
-                const int sw = (c ^ (h & 3)) << 4;  // 64-byte swizzle: rows 2h, 2h+1 share (row >> 1) & 3
-                *reinterpret_cast<uint4*>(tile + (2 * h) * 64 + sw) = make_uint4(hi0.x, hi0.y, hi1.x, hi1.y);
-                *reinterpret_cast<uint4*>(tile + (2 * h + 1) * 64 + sw) = make_uint4(lo0.x, lo0.y, lo1.x, lo1.y);
+                const int sw = (c ^ ((h >> 1) & 3)) << 4;  // 64-byte swizzle: 16-byte chunk c of row h
+                *reinterpret_cast<uint4*>(tile + h * 64 + sw) = make_uint4(hi0.x, hi0.y, hi1.x, hi1.y);
+                *reinterpret_cast<uint4*>(tile + kQHalfBytes + h * 64 + sw) = make_uint4(lo0.x, lo0.y, lo1.x, lo1.y);
             }
             ctl.wq[qs][h] = wraw[rs * kHeads + h] * s_h;
             mbar_arrive(&ctl.qraw_empty[rs]);
@@ -501,28 +510,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
             {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr, r);  // heads 0-15: hi, lo interleaved
-                tmem_ld_wait(r);
-#pragma unroll
-                for (int h = 0; h < 16; h += 2) {
-                    const float d0 = fmaf(__uint_as_float(r[2 * h + 1]), 0.0625f, __uint_as_float(r[2 * h]));
-                    const float d1 = fmaf(__uint_as_float(r[2 * h + 3]), 0.0625f, __uint_as_float(r[2 * h + 2]));
-                    s0 = fmaf(wv[h], fmaxf(d0, 0.f), s0);
-                    s1 = fmaf(wv[h + 1], fmaxf(d1, 0.f), s1);
-                }
-            }
-            {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + 32, r);  // heads 16-31
+                tmem_ld_32x32b_x32(taddr, r);  // acc[h], h = 0..31
                 tmem_ld_wait(r);
                 tc_fence_before_sync();
                 mbar_arrive(&ctl.tempty[acc]);
+                const float4* w4 = reinterpret_cast<const float4*>(wv);
 #pragma unroll
-                for (int h = 0; h < 16; h += 2) {
-                    const float d2 = fmaf(__uint_as_float(r[2 * h + 1]), 0.0625f, __uint_as_float(r[2 * h]));
-                    const float d3 = fmaf(__uint_as_float(r[2 * h + 3]), 0.0625f, __uint_as_float(r[2 * h + 2]));
-                    s2 = fmaf(wv[16 + h], fmaxf(d2, 0.f), s2);
-                    s3 = fmaf(wv[17 + h], fmaxf(d3, 0.f), s3);
+                for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+                    const float4 wq = w4[h4];
+                    s0 = fmaf(wq.x, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f), s0);
+                    s1 = fmaf(wq.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), s1);
+                    s2 = fmaf(wq.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), s2);
+                    s3 = fmaf(wq.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), s3);
                 }
             }
             const float s = key_scale * ((s0 + s1) + (s2 + s3));

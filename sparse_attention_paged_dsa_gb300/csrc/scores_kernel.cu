@@ -41,9 +41,10 @@
 //   * kEpiGroups groups of 4 warps (group g takes every kEpiGroups-th unit)
 //     read the accumulators with tcgen05.ld (thread = key row, registers =
 //     32 heads), apply relu, the head weights and the head sum in registers,
-//     mask, and store 128 contiguous fp32 scores per unit.  Before that they
-//     stream -inf over the dead part of every row (split over all CTAs) when
-//     a full-width row is requested.
+//     mask, and store 128 contiguous fp32 scores per unit.
+//   * Warp 3 builds the per-request table of live counts and unit offsets;
+//     when a full-width row is requested it then streams -inf over the dead
+//     part of every row (an equal share per CTA), beside the pipeline.
 //   * Programmatic dependent launch: barrier and TMEM set-up overlap the tail
 //     of the previous kernel; global memory is touched only after
 //     griddepcontrol.wait.
@@ -172,7 +173,10 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
     const uint32_t tmem_base = ctl.tmem_base;
     const int64_t M = p.row_width;
 
-    if (warp == 0 || warp == 2) {
+    if (warp == 3) {
+        // ================= set-up warp, then the -inf fill of the rows' dead parts (full-width rows) =================
+        if (p.fill_dead) fill_dead_tails_warp(ctl.rows, p, lane, Q);
+    } else if (warp == 0 || warp == 2) {
         // ================= producers: warp 0 issues the CTA's even units, warp 2 the odd ones =================
         // Both walk the same unit sequence (page ids fetched one batch ahead); a row change is
         // numbered in sequence order and warp 0 loads every row's query tile, in that order, so
@@ -349,7 +353,6 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
         const int quad = warp & 3;          // TMEM lanes [32*quad, 32*quad + 32)
         const float neg_inf = __int_as_float(0xff800000);
 
-        if (p.fill_dead) fill_dead_tails(ctl.rows, p, et, kEpiThreads, Q);
 
         int cur_b = -1, n = 0;
         int n_tok[Q];  // live keys of each token of the current request

@@ -12,11 +12,12 @@
 // k-th largest score and how many keys equal to T are taken (the lowest
 // positions); every key > T and those keys == T are written in ascending
 // position.  One 1024-thread CTA per request.
-//   * n_b <= 32768, first choice (sampled path): keys stay in registers in
-//     load order; a histogram of every 4th key gives a threshold that keeps a
-//     little more than k keys; those are compacted, in position order, into a
-//     short list in shared memory, and the radix passes and the ordered write
-//     run on that list only.
+//   * n_b <= 32768, first choice (sampled path): the row is copied into shared
+//     memory by the bulk-copy engine; a histogram of every 4th key gives a
+//     threshold that keeps a little more than k keys; those are appended with
+//     their positions to a short list, the radix passes run on that list
+//     only, and the selected positions are marked in bitmaps whose prefix
+//     counts place each one in ascending order.
 //   * n_b <= 32768 when the sample misjudges (fewer than k or too many keys
 //     pass): each thread holds 32 consecutive keys (transposed through padded
 //     shared memory); the radix passes run over all keys in registers and
@@ -41,17 +42,25 @@ constexpr int kCacheCap = 49152;                    // keys held in shared memor
 constexpr int kKeysPerThread = 32;                  // register path: keys per thread
 constexpr int kRegCap = kThreads * kKeysPerThread;  // 32768
 constexpr int kLoadsPerThread = kRegCap / 4 / kThreads;  // float4 loads per thread on the register path
+constexpr int kCandCap = 8192;                      // sampled path: candidate list capacity
 
 struct TopkSmem {
+    uint64_t row_bar;                            // sampled path: the row's bulk copy
+    int abort;                                   // never set (bounded waits read it)
+    uint32_t ncand;                              // sampled path: candidates appended
     uint32_t hist[2048];
     uint32_t warp_tot[kWarps];
     uint32_t warp_gt[kWarps];
     uint32_t warp_eq[kWarps];
     uint32_t result[2];
     uint32_t hist2[2048];                        // second histogram buffer (list pass 2)
-    uint32_t chunk_tot[kLoadsPerThread];         // candidates per 4096-position chunk
-    uint32_t wpre[kLoadsPerThread][kWarps];      // candidates per (chunk, warp), then their prefix in the chunk
+    uint32_t bits_gt[kRegCap / 32];              // sampled path: positions with key > T
+    uint32_t bits_eq[kRegCap / 32];              // sampled path: positions with key == T
 };
+
+// Shared-memory words the sampled path needs for a row of n keys: the row,
+// rounded up to whole groups of four, then the candidate list (keys, positions).
+__host__ __device__ constexpr int sampled_row_words(int n) { return (n + 3) & ~3; }
 
 // Find the bin holding the kk-th largest key: result[0] = bin,
 // result[1] = how many keys of that bin are still to be taken.  Ends with a
@@ -178,8 +187,9 @@ __device__ __forceinline__ void select_row_small(TopkSmem& sm, uint32_t* keys, c
 // thread i reading its key j hits bank (i + j) % 32.
 __device__ __forceinline__ int pad_slot(int p) { return p + (p >> 5); }
 
-__device__ __forceinline__ void select_row_regs(TopkSmem& sm, uint32_t* stage, const float* __restrict__ row, int n,
-                                                int k, int32_t* __restrict__ out) {
+// Not inlined: the fallback of the sampled path, kept out of its register budget.
+__device__ __noinline__ void select_row_regs(TopkSmem& sm, uint32_t* stage, const float* __restrict__ row, int n,
+                                             int k, int32_t* __restrict__ out) {
     const int tid = threadIdx.x;
     clear_hist(sm);
 
@@ -266,126 +276,127 @@ __device__ __forceinline__ void select_row_regs(TopkSmem& sm, uint32_t* stage, c
 }
 
 // ------------------------------------------------------------ sampled path
-// Rows of up to 32768 live positions.  Keys stay in registers in load order
-// (thread t holds positions 4 (t + 1024 j) + c).  Every 4th position is a
-// sample; the bin of the sample histogram that holds rank r (the expected
-// rank of the k-th largest among the samples plus four standard deviations)
-// gives a threshold tau that all but rarely keeps at least k keys.  Keys >= tau
-// are compacted in position order into shared memory, the exact 3-pass radix
-// select runs on that short list, and the output is an ordered filter of it.
-// Returns false, with nothing written, when fewer than k or more keys than the
-// list holds pass tau; the caller then runs the exact full-row path.
-__device__ __forceinline__ bool select_row_sampled(TopkSmem& sm, uint32_t* buf, int buf_words,
-                                                   const float* __restrict__ row, int n, int k,
-                                                   int32_t* __restrict__ out) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int kChunks = kLoadsPerThread;
-    clear_hist(sm);
+// Rows of up to 32768 live positions.  One thread copies the row's whole
+// groups of four into shared memory with bulk copies (the last partial group
+// by plain loads); thread t then reads groups t + 1024 j, positions
+// 4 (t + 1024 j) + c.  The first key of every group is a sample; the bin of
+// the sample histogram that holds rank r (the expected rank of the k-th
+// largest among the samples plus four standard deviations) gives a threshold
+// tau that all but rarely keeps at least k keys.  Keys >= tau are appended,
+// with their positions and in no particular order, to a list after the row;
+// the exact 3-pass radix select runs on that list; the selected positions are
+// set in two bitmaps (key > T, key == T), and one block scan of the bitmap
+// words' bit counts gives every selected position its output slot, in
+// ascending position with the lowest positions of key T taken first.
+// Returns 1 when the row is done, 0 (nothing written) when fewer than k or
+// more keys than the list holds pass tau -- the caller then runs the exact
+// full-row path -- and -1 when the row's copy did not land within the wait
+// limit (error bit set, the row padded with -1).
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(sdst)),
+                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 
-    uint32_t key[kKeysPerThread];  // key[4 j + c]: position 4 (tid + kThreads j) + c
-    const int n4 = n >> 2;
-    const float4* row4 = reinterpret_cast<const float4*>(row);
-#pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
-        const int i = tid + j * kThreads;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < n4) {
-            v = __ldcg(row4 + i);
-        } else if (i == n4) {  // the last, partial group of four
-            const int r = n - 4 * n4;
-            if (r > 0) v.x = __ldcg(row + 4 * i);
-            if (r > 1) v.y = __ldcg(row + 4 * i + 1);
-            if (r > 2) v.z = __ldcg(row + 4 * i + 2);
-        }
-        key[4 * j + 0] = order_key(v.x);
-        key[4 * j + 1] = order_key(v.y);
-        key[4 * j + 2] = order_key(v.z);
-        key[4 * j + 3] = order_key(v.w);
+__device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, int buf_words,
+                                                  const float* __restrict__ row, int n, int k,
+                                                  int32_t* __restrict__ out, uint32_t* err) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int row_words = sampled_row_words(n);
+    const int cap = min(kCandCap, (buf_words - row_words) / 2);
+    if (cap < k) return 0;
+    const int n4 = n >> 2;        // whole groups
+    const int ng = row_words >> 2;  // groups, the last one possibly partial
+    float* rs = reinterpret_cast<float*>(buf);
+    uint32_t* cand_key = buf + row_words;
+    uint32_t* cand_pos = cand_key + cap;
+
+    if (tid == 0) {
+        mbar_init(&sm.row_bar, 1);
+        fence_mbar_init();
+        sm.abort = 0;
+        sm.ncand = 0;
     }
-    __syncthreads();  // histogram cleared
-
-    // Sample histogram: positions 4 i (the first key of each group of four).
-#pragma unroll
-    for (int j = 0; j < kChunks; ++j)
-        if (4 * (tid + j * kThreads) < n) atomicAdd(&sm.hist[key[4 * j] >> 21], 1u);
+    if (tid < 4 && 4 * n4 + tid < row_words)  // the partial group: live scores, then zeros
+        rs[4 * n4 + tid] = 4 * n4 + tid < n ? __ldcg(row + 4 * n4 + tid) : 0.f;
+    clear_hist(sm);
+    sm.bits_gt[tid] = 0;
+    sm.bits_eq[tid] = 0;
     __syncthreads();
-    const int ns = (n + 3) >> 2;
-    const float expect = float(k) * float(ns) / float(n);
-    const int r = min(ns, int(expect + 4.f * sqrtf(expect)) + 8);
+    if (tid == 0) {
+        constexpr uint32_t kChunk = 32768;
+        const uint32_t bytes = uint32_t(n4) * 16u;
+        mbar_arrive_expect_tx(&sm.row_bar, bytes);
+        for (uint32_t off = 0; off < bytes; off += kChunk)
+            bulk_load(reinterpret_cast<uint8_t*>(rs) + off, reinterpret_cast<const uint8_t*>(row) + off,
+                      min(kChunk, bytes - off), &sm.row_bar);
+    }
+    const bool landed = mbar_wait(&sm.row_bar, 0, &sm.abort);
+    if (__syncthreads_or(!landed)) {
+        if (tid == 0) atomicOr(err, kErrWaitTimeout);
+        for (int i = tid; i < k; i += kThreads) out[i] = -1;
+        if (!landed) mbar_wait(&sm.row_bar, 0, &sm.abort);  // once more (bounded) for the copy in flight
+        return -1;
+    }
+
+    // Sample histogram: the first key of every group (position 4 g < n).
+    const float4* rs4 = reinterpret_cast<const float4*>(rs);
+#pragma unroll
+    for (int j = 0; j < kLoadsPerThread; ++j) {
+        const int g = tid + j * kThreads;
+        if (g < ng) atomicAdd(&sm.hist[order_key(rs4[g].x) >> 21], 1u);
+    }
+    __syncthreads();
+    const float expect = float(k) * float(ng) / float(n);
+    const int r = min(ng, int(expect + 4.f * sqrtf(expect)) + 8);
     select_bin<2048>(sm, uint32_t(r));
     const uint32_t tau = sm.result[0] << 21;
 
-    // Candidates per chunk, ordered prefix over (chunk, warp, lane, c).
-    uint32_t lo = 0, hi = 0;  // 8-bit counts of chunks 0-3 and 4-7
+    // Candidates: bit 4 j + c of `flags` marks position 4 (tid + 1024 j) + c.  The test
+    // key(v) >= tau is made in fp32 as v >= f_tau, which is the same for every non-NaN v
+    // (-0 == +0 on both sides); the unordered compare also admits every NaN and, when tau
+    // lies past +inf, +inf itself.  Extra candidates are harmless as long as the k-th
+    // largest key of the list is >= tau, which is checked after the radix passes.
+    const float f_tau = tau < 0x00800000u   ? __int_as_float(0xff800000)  // every non-NaN key >= tau
+                        : tau > 0xFF800000u ? __int_as_float(0x7f800000)
+                        : (tau & 0x80000000u) ? __uint_as_float(tau & 0x7FFFFFFFu)
+                                              : __uint_as_float(~tau);
+    uint32_t flags = 0;
 #pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
-        uint32_t c = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) c += (4 * (tid + j * kThreads) + q < n && key[4 * j + q] >= tau) ? 1u : 0u;
-        if (j < 4)
-            lo |= c << (8 * j);
-        else
-            hi |= c << (8 * (j - 4));
+    for (int j = 0; j < kLoadsPerThread; ++j) {
+        const int g = tid + j * kThreads;
+        const int live = n - 4 * g;  // > 3: the whole group
+        const float4 v = g < ng ? rs4[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t f = (live > 0 && !(v.x < f_tau) ? 1u : 0u) | (live > 1 && !(v.y < f_tau) ? 2u : 0u) |
+                           (live > 2 && !(v.z < f_tau) ? 4u : 0u) | (live > 3 && !(v.w < f_tau) ? 8u : 0u);
+        flags |= f << (4 * j);
     }
-    uint32_t lo_in = lo, hi_in = hi;
+    const uint32_t cnt = __popc(flags);
+    uint32_t incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t x = __shfl_up_sync(0xffffffffu, lo_in, o);
-        const uint32_t y = __shfl_up_sync(0xffffffffu, hi_in, o);
-        if (lane >= o) {
-            lo_in += x;
-            hi_in += y;
-        }
+        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
     }
-    if (lane == 31) {
-#pragma unroll
-        for (int j = 0; j < kChunks; ++j)
-            sm.wpre[j][warp] = ((j < 4 ? lo_in : hi_in) >> (8 * (j & 3))) & 0xFFu;
+    uint32_t base = 0;
+    if (lane == 31) base = atomicAdd(&sm.ncand, incl);
+    uint32_t slot = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+    while (flags) {
+        const int i = __ffs(flags) - 1;
+        flags &= flags - 1u;
+        const int pos = 4 * (tid + kThreads * (i >> 2)) + (i & 3);
+        if (slot < uint32_t(cap)) {
+            cand_key[slot] = order_key(rs[pos]);
+            cand_pos[slot] = uint32_t(pos);
+        }
+        ++slot;
     }
     __syncthreads();
-    if (warp < kChunks) {  // warp j: exclusive prefix over the warps of chunk j
-        const uint32_t v = sm.wpre[warp][lane];
-        uint32_t s = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t x = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += x;
-        }
-        sm.wpre[warp][lane] = s - v;
-        if (lane == 31) sm.chunk_tot[warp] = s;
-    }
-    __syncthreads();
-    uint32_t total = 0;
-    uint32_t chunk_off[kChunks];
-#pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
-        chunk_off[j] = total;
-        total += sm.chunk_tot[j];
-    }
-    const int cap = min(16384, buf_words / 2);
-    if (total < uint32_t(k) || total > uint32_t(cap)) return false;
+    const int C = int(sm.ncand);
+    if (C < k || C > cap) return 0;
 
-    uint32_t* cand_key = buf;
-    uint32_t* cand_pos = buf + cap;
-#pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
-        const uint32_t incl = ((j < 4 ? lo_in : hi_in) >> (8 * (j & 3))) & 0xFFu;
-        const uint32_t own = ((j < 4 ? lo : hi) >> (8 * (j & 3))) & 0xFFu;
-        uint32_t slot = chunk_off[j] + sm.wpre[j][warp] + incl - own;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int pos = 4 * (tid + j * kThreads) + q;
-            if (pos < n && key[4 * j + q] >= tau) {
-                cand_key[slot] = key[4 * j + q];
-                cand_pos[slot] = uint32_t(pos);
-                ++slot;
-            }
-        }
-    }
-    const int C = int(total);
-
-    // Exact selection on the list (already in position order).  Pass 1 uses hist, pass 2 hist2
-    // (cleared with hist), pass 3 hist again.
+    // Exact selection on the list.  Pass 1 uses hist, pass 2 hist2 (cleared with hist), pass 3 hist again.
     clear_hist(sm);
     for (int i = tid; i < 2048; i += kThreads) sm.hist2[i] = 0;
     __syncthreads();
@@ -412,29 +423,33 @@ __device__ __forceinline__ bool select_row_sampled(TopkSmem& sm, uint32_t* buf, 
     select_bin<1024>(sm, kk);
     const uint32_t T = (prefix22 << 10) | sm.result[0];
     const uint32_t take_eq = sm.result[1];
+    if (T < tau) return 0;  // the list's extra candidates (NaN, +inf) reached rank k
 
-    // Ordered filter: thread t owns list entries [t * per, t * per + per).
-    const int per = (C + kThreads - 1) / kThreads;
-    const int i0 = min(C, tid * per), i1 = min(C, i0 + per);
-    uint32_t gt = 0, eq = 0;
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t ck = cand_key[i];
-        gt += ck > T ? 1u : 0u;
-        eq += ck == T ? 1u : 0u;
+    // Mark the selected positions, then write them in ascending order: thread t owns
+    // bitmap word t (positions 32 t .. 32 t + 31).
+    for (int i = tid; i < C; i += kThreads) {
+        const uint32_t ck = cand_key[i], pos = cand_pos[i];
+        if (ck > T)
+            atomicOr(&sm.bits_gt[pos >> 5], 1u << (pos & 31u));
+        else if (ck == T)
+            atomicOr(&sm.bits_eq[pos >> 5], 1u << (pos & 31u));
     }
-    uint32_t gt_run, eq_run;
-    block_scan2(sm, gt, eq, gt_run, eq_run);
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t ck = cand_key[i];
-        if (ck > T) {
-            out[gt_run + min(eq_run, take_eq)] = int32_t(cand_pos[i]);
-            ++gt_run;
-        } else if (ck == T) {
-            if (eq_run < take_eq) out[gt_run + eq_run] = int32_t(cand_pos[i]);
-            ++eq_run;
-        }
+    __syncthreads();
+    const uint32_t g = sm.bits_gt[tid], e = sm.bits_eq[tid];
+    uint32_t g_before, e_before;
+    block_scan2(sm, __popc(g), __popc(e), g_before, e_before);
+    uint32_t m = g;
+    for (uint32_t ee = e, c = e_before; ee != 0u && c < take_eq; ++c) {  // the lowest equal keys still wanted
+        m |= ee & (0u - ee);
+        ee &= ee - 1u;
     }
-    return true;
+    uint32_t at = g_before + min(e_before, take_eq);
+    while (m) {
+        const int bit = __ffs(m) - 1;
+        m &= m - 1u;
+        out[at++] = 32 * tid + bit;
+    }
+    return 1;
 }
 
 // ------------------------------------------------------- long-row path
@@ -554,7 +569,7 @@ __device__ __forceinline__ void select_row(TopkSmem& sm, uint32_t* cache, const 
 }
 
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, int cache_cap) {
-    extern __shared__ uint32_t cache[];
+    extern __shared__ __align__(16) uint32_t cache[];
     __shared__ TopkSmem sm;
     // Launched as a programmatic dependent of the scores kernel: wait for its
     // results before touching global memory.
@@ -578,7 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
         return;
     }
     if (n <= kRegCap && pad_slot(n) <= cache_cap) {
-        if (!select_row_sampled(sm, cache, cache_cap, row, n, k, out)) {
+        const int done = select_row_sampled(sm, cache, cache_cap, row, n, k, out, p.err);
+        if (done == 0) {
             __syncthreads();
             select_row_regs(sm, cache, row, n, k, out);
         }
@@ -592,8 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
 }  // namespace
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
-    // Shared keys: the row (padded by one word per 32 for the register path), capped at kCacheCap.
-    const int64_t want = p.row_width + p.row_width / 32 + 1;
+    // Shared keys: the larger of the row padded by one word per 32 (register path) and the
+    // row plus a candidate list (sampled path), capped at kCacheCap.
+    const int64_t padded = p.row_width + p.row_width / 32 + 1;
+    const int64_t cand = p.row_width < kCandCap ? p.row_width : kCandCap;
+    const int64_t sampled = ((p.row_width + 3) & ~int64_t(3)) + 2 * cand;
+    const int64_t want = padded > sampled ? padded : sampled;
     const int cache_cap = p.row_width > p.k ? int(want < kCacheCap ? want : kCacheCap) : 0;
     const size_t smem = size_t(cache_cap) * sizeof(uint32_t);
     static SmemLimitOnce smem_limit;

@@ -200,6 +200,33 @@ def test_topk_rows_that_defeat_the_sample(gpu_lib, oracle):
         np.testing.assert_array_equal(got[i], ref, err_msg=f"row {i}")
 
 
+def test_topk_infinite_scores(gpu_lib, oracle):
+    """Rows holding +inf and -inf scores (a caller's row through dsa_indexer_topk): more +inf
+    keys than k (the threshold sits at +inf and ties resolve to the lower positions), a few +inf
+    among many -inf, and a row whose k-th largest score is -inf."""
+    rng = np.random.default_rng(4321)
+    M, k = 32768, 2048
+    rows, n_live = [], []
+    r = rng.standard_normal(M).astype(np.float32)
+    r[rng.choice(M, 3000, replace=False)] = np.inf
+    rows.append(r); n_live.append(M)
+    r = rng.standard_normal(M).astype(np.float32)
+    r[rng.choice(M, 20000, replace=False)] = -np.inf
+    r[rng.choice(M, 100, replace=False)] = np.inf
+    rows.append(r); n_live.append(M)
+    r = np.full(M, -np.inf, np.float32)
+    r[rng.choice(M, 1000, replace=False)] = rng.standard_normal(1000).astype(np.float32)
+    rows.append(r); n_live.append(M)
+    r = rng.standard_normal(M).astype(np.float32)
+    r[rng.choice(29999, 2500, replace=False)] = np.inf
+    rows.append(r); n_live.append(29999)                    # ragged tail
+    rows = np.stack(rows)
+    got = _topk_on_rows(gpu_lib, rows, n_live, k)
+    for i, n in enumerate(n_live):
+        ref = oracle.topk_row(rows[i].astype(np.float64), n, k)
+        np.testing.assert_array_equal(got[i], ref, err_msg=f"row {i}")
+
+
 def _signed_zero_rows(rng, M):
     """Rows whose k-th largest score is 0 and that hold both +0 and -0 (equal in fp32 order,
     so they tie and go to the lower position whatever their sign)."""
