@@ -302,8 +302,10 @@ DSA_API dsa_status_t dsa_indexer_qw_proj(const void *x, const void *w_q, const v
  *              header zeroed once (dsa_indexer_workspace_init); holds the error word
  *              and the per-split partial outputs (sized for the current device).
  * Asynchronous on `stream`; allocates nothing.  A live page id outside
- * [0, num_pages) sets DSA_DEVERR_BAD_PAGE and that entry is read as zeros;
- * results are unspecified while the error word is non-zero. */
+ * [0, num_pages) sets DSA_DEVERR_BAD_PAGE and that page is not read (another
+ * of the request's rows stands in for the entry); results are unspecified
+ * while the error word is non-zero.  num_pages above 2^25 - 1 (cache rows
+ * past 32-bit coordinates) returns DSA_ERR_UNSUPPORTED. */
 #define DSA_MLA_HEADS 64
 #define DSA_MLA_DIM 576
 #define DSA_MLA_DV 512

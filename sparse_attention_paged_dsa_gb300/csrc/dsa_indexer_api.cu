@@ -543,8 +543,12 @@ dsa_status_t dsa_sparse_mla_decode(const void* q, const void* kv_cache, int64_t 
     st = check_workspace(workspace, workspace_bytes,
                          dsa::kWorkspaceHeaderBytes + mla_partial_floats(batch, splits) * sizeof(float));
     if (st != DSA_OK) return st;
-    CUtensorMap q_map;
+    // The row gathers address cache rows with 32-bit coordinates.
+    if (num_pages > (int64_t(1) << 31) / dsa::kPageEntries - 1) return DSA_ERR_UNSUPPORTED;
+    CUtensorMap q_map, kv_map;
     st = make_rows_map(&q_map, q, int64_t(batch) * DSA_MLA_HEADS, DSA_MLA_DIM, 64, "mla q");
+    if (st != DSA_OK) return st;
+    st = make_rows_map(&kv_map, kv_cache, num_pages * dsa::kPageEntries, DSA_MLA_DIM, 1, "mla kv");
     if (st != DSA_OK) return st;
     dsa::MlaParams p{};
     p.kv = static_cast<const uint8_t*>(kv_cache);
@@ -564,7 +568,7 @@ dsa_status_t dsa_sparse_mla_decode(const void* q, const void* kv_cache, int64_t 
     p.k = k;
     p.splits = splits;
     p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
-    const cudaError_t e = dsa::launch_mla(q_map, p, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = dsa::launch_mla(q_map, kv_map, p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "sparse MLA decode launch");
 }
 }  // extern "C"

@@ -133,6 +133,8 @@ struct MlaParams {
 size_t mla_smem_bytes();
 // Decode kernel (grid splits x batch) and, for splits > 1, the log-sum-exp merge.
 // q_map: q [batch * 64, 576] bf16, 128-byte-swizzled boxes of 64 x 64.
-cudaError_t launch_mla(const CUtensorMap& q_map, const MlaParams& p, cudaStream_t stream);
+// kv_map: the cache as [num_pages * 64, 576] bf16 rows, 128-byte-swizzled boxes of
+// one row x 64 (the row gathers' map).
+cudaError_t launch_mla(const CUtensorMap& q_map, const CUtensorMap& kv_map, const MlaParams& p, cudaStream_t stream);
 
 }  // namespace dsa

@@ -13,10 +13,13 @@
 // One CTA per (split, request), one CTA per SM (all of shared memory and
 // TMEM).  The request's non-empty 64-entry blocks of the top-k row are divided
 // into `splits` contiguous ranges; a CTA streams its blocks:
-//   * warps 0, 2, 3: gather every block's 64 entries with 16-byte cp.async
-//     into nine 128-byte-swizzled slabs of 64 rows x 64 dims (a ring of 8 slab
-//     pairs for the 512 value dims, 2 slabs for the rotary 64); each warp
-//     copies a third of every slab's rows; unused entries are zero-filled.
+//   * warps 0, 2, 3: gather every block's 64 entries by TMA row gathers
+//     (tile::gather4: four cache rows of 64 dims per instruction, from a
+//     tensor map over the cache viewed as [pages x 64 rows, 576]) into nine
+//     128-byte-swizzled slabs of 64 rows x 64 dims (a ring of 8 slab pairs for
+//     the 512 value dims, 2 slabs for the rotary 64); each warp gathers a
+//     third of every slab's 4-row groups, one group per lane.  Unused entries
+//     repeat the row of the block's first used entry (their weights are 0).
 //     Warp 0 also loads q once by TMA.
 //   * warp 1: tcgen05.mma kind::f16 --
 //       MMA1  S[head, entry] = Q . K^T, M = 64 heads, N = 64 entries, K = 576
@@ -35,10 +38,9 @@
 // is bounded (about 1 s); a timeout sets an error bit, the roles drain, and
 // TMEM is freed.
 //
-// What bounds it: a gathered row is 9 separate 128-byte segments, and 16-byte
-// cp.async moves at most about 40 GB/s per SM on this part, with a loaded
-// latency of about 4 us; a 2-block ring (all the shared memory beside q) holds
-// one block in flight while the previous one is computed.
+// What bounds it: a gathered row is 9 separate 128-byte segments; a 2-block
+// ring (all the shared memory beside q) holds one block in flight while the
+// previous one is computed.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -64,8 +66,8 @@ constexpr int kOffV = kOffP + kSlabBytes;
 constexpr int kOffR = kOffV + kVRing * kPairBytes;
 constexpr int kOffCtl = kOffR + kRRing * kSlabBytes;
 constexpr int kThreadsM = 256;
-constexpr int kProducers = 3;    // warps 0, 2, 3: each copies row groups k = p, p + 3, ... of every slab
-constexpr int kRowGroups = 16;   // 4 rows x 128 bytes per warp-wide cp.async
+constexpr int kProducers = 3;    // warps 0, 2, 3: each gathers row groups k = p, p + 3, ... of every slab
+constexpr int kRowGroups = 16;   // 4 rows x 128 bytes per gather
 constexpr uint32_t kTmemColsM = 512;
 constexpr uint32_t kColS = 0;    // S: 64 columns
 constexpr uint32_t kColO = 128;  // O^T: 4 x 64 columns
@@ -127,12 +129,24 @@ __device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t b
                  : "memory");
 }
 
-// 16-byte copy global -> shared through L2; src_bytes 0 writes zeros and reads nothing.
-__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+// TMA row gather: rows y0..y3 of a 2-D tensor map (box = one row of 64 bf16), columns
+// [x, x + 64), into 4 x 128 bytes at `dst` (swizzled by the map, like a 4-row tile).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
+                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)),
+        "l"(policy)
+        : "memory");
 }
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+
+// Bounded wait for a phase of `bar` (only while draining after an abort).
+__device__ __forceinline__ void wait_landed_m(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
+    }
 }
 
 // Named barrier over the 128 softmax threads returning the OR of `v`.
@@ -158,7 +172,8 @@ __device__ __forceinline__ int entry_pos(const MlaParams& p, int b, int e, int n
 }
 
 __global__ void __launch_bounds__(kThreadsM, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap q_map, const MlaParams p) {
+    mla_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
+                      const MlaParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     MlaCtl& ctl = *reinterpret_cast<MlaCtl*>(tiles + kOffCtl);
@@ -171,11 +186,11 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kVRing; ++i) {
-            mbar_init(&ctl.v_full[i], 32 * kProducers);  // one noinc arrival per producer lane
+            mbar_init(&ctl.v_full[i], kProducers);  // one expect-tx arrival per producer warp
             mbar_init(&ctl.v_empty[i], 1);
         }
         for (int i = 0; i < kRRing; ++i) {
-            mbar_init(&ctl.r_full[i], 32 * kProducers);
+            mbar_init(&ctl.r_full[i], kProducers);
             mbar_init(&ctl.r_empty[i], 1);
         }
         mbar_init(&ctl.q_full, 1);
@@ -186,6 +201,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         ctl.blk_mask = 0;
         fence_mbar_init();
         tma_prefetch_map(&q_map);
+        tma_prefetch_map(&kv_map);
     }
     if (warp == 1) {
         tmem_alloc(&ctl.tmem_base, kTmemColsM);
@@ -237,7 +253,6 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     if (warp == 0 || warp == 2 || warp == 3) {
         // ================= producers: gather the blocks' entries =================
         const int pw = warp == 0 ? 0 : warp - 1;
-        const uint8_t* kv = p.kv;
         bool stop = false;
         if (warp == 0 && lane == 0 && nblk > 0) {
             mbar_arrive_expect_tx(&ctl.q_full, uint32_t(kQSlabs * kSlabBytes));
@@ -245,33 +260,44 @@ __global__ void __launch_bounds__(kThreadsM, 1)
             for (int s = 0; s < kQSlabs; ++s)
                 tma_load_2d(tiles + kOffQ + s * kSlabBytes, &q_map, &ctl.q_full, s * 64, b * kMlaHeads, pol);
         }
-        const int c = lane & 7;  // 16-byte chunk of a 128-byte slab row
+        const uint64_t pol_kv = l2_policy_evict_first();
+        // Lane i < ngw gathers row group k = pw + 3 i (rows 4k .. 4k + 3) of every slab.
+        const int ngw = (kRowGroups - pw + kProducers - 1) / kProducers;
+        const int k = pw + kProducers * lane;
+        int last_v = -1, last_r = -1;  // the last value / rotary fills this warp took part in
 #pragma unroll 1
         for (int n = 0; n < nblk && !stop; ++n) {
             const int blk = ctl.blocks[n];
-            // byte offsets of entries lane and lane + 32 (-1: unused, zero-filled)
-            int64_t off[2];
+            // cache rows of entries lane and lane + 32 (-1: unused or on a bad page)
+            int row[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int t = entry_pos(p, b, blk * kBlk + h * 32 + lane, n_live);
-                off[h] = -1;
+                row[h] = -1;
                 if (t >= 0) {
                     const int page = __ldg(p.page_table + int64_t(b) * p.table_width + (t >> 6));
                     if (page >= 0 && int64_t(page) < p.num_pages)
-                        off[h] = (int64_t(page) * kPageEntries + (t & 63)) * (kMlaDim * 2);
+                        row[h] = page * kPageEntries + (t & 63);
                     else
                         atomicOr(p.err, kErrBadPage);
                 }
             }
-            // this lane copies chunk c of rows r = 4 k + lane / 8 for its row groups k = pw + 3 i
-            constexpr int kMaxGroups = (kRowGroups + kProducers - 1) / kProducers;
-            int64_t row_off[kMaxGroups];
+            // Rows of unused entries repeat the block's first used row (row 0 if none is readable):
+            // every gathered row is one the request uses, and its softmax weight there is 0.
+            const uint32_t u0 = __ballot_sync(0xffffffffu, row[0] >= 0);
+            const uint32_t u1 = __ballot_sync(0xffffffffu, row[1] >= 0);
+            const int f0 = __shfl_sync(0xffffffffu, row[0], u0 ? __ffs(u0) - 1 : 0);
+            const int f1 = __shfl_sync(0xffffffffu, row[1], u1 ? __ffs(u1) - 1 : 0);
+            const int first = u0 ? f0 : (u1 ? f1 : 0);
+            row[0] = row[0] >= 0 ? row[0] : first;
+            row[1] = row[1] >= 0 ? row[1] : first;
+            int y[4];  // rows of this lane's group (entries 4k .. 4k + 3)
 #pragma unroll
-            for (int i = 0; i < kMaxGroups; ++i) {
-                const int k = pw + kProducers * i;
-                const int r = 4 * k + (lane >> 3);
-                const int64_t v = k < 8 ? off[0] : off[1];
-                row_off[i] = __shfl_sync(0xffffffffu, v, r & 31);  // k is warp-uniform
+            for (int c = 0; c < 4; ++c) {
+                const int e = 4 * k + c;
+                const int a0 = __shfl_sync(0xffffffffu, row[0], e & 31);
+                const int a1 = __shfl_sync(0xffffffffu, row[1], e & 31);
+                y[c] = e < 32 ? a0 : a1;
             }
 #pragma unroll 1
             for (int j = 0; j <= 4; ++j) {  // value pairs 0..3, then the rotary slab
@@ -280,7 +306,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                 int nslabs, slab0;
                 if (j < 4) {
                     const int pos = 4 * n + j, slot = pos & (kVRing - 1), use = pos / kVRing;
-                    const bool ok = mbar_wait(&ctl.v_empty[slot], uint32_t(use & 1) ^ 1u, &ctl.abort);
+                    const bool ok = lane != 0 || mbar_wait(&ctl.v_empty[slot], uint32_t(use & 1) ^ 1u, &ctl.abort);
                     if (!__all_sync(0xffffffffu, ok)) {  // the lanes stop together
                         stop = true;
                         break;
@@ -289,9 +315,10 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                     dst_base = s_base + kOffV + slot * kPairBytes;
                     nslabs = 2;
                     slab0 = 2 * j;
+                    last_v = pos;
                 } else {
                     const int slot = n & (kRRing - 1), use = n / kRRing;
-                    const bool ok = mbar_wait(&ctl.r_empty[slot], uint32_t(use & 1) ^ 1u, &ctl.abort);
+                    const bool ok = lane != 0 || mbar_wait(&ctl.r_empty[slot], uint32_t(use & 1) ^ 1u, &ctl.abort);
                     if (!__all_sync(0xffffffffu, ok)) {
                         stop = true;
                         break;
@@ -300,30 +327,28 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                     dst_base = s_base + kOffR + slot * kSlabBytes;
                     nslabs = 1;
                     slab0 = 8;
+                    last_r = n;
                 }
-                for (int hs = 0; hs < nslabs; ++hs) {
-                    const int s = slab0 + hs;
-                    const uint32_t slab = dst_base + hs * kSlabBytes;
-#pragma unroll
-                    for (int i = 0; i < kMaxGroups; ++i) {
-                        const int k = pw + kProducers * i;
-                        if (k >= kRowGroups) break;
-                        const int r = 4 * k + (lane >> 3);
-                        const uint32_t dst = slab + r * 128 + ((c ^ (r & 7)) << 4);
-                        const bool use_row = row_off[i] >= 0;
-                        const uint8_t* src = use_row ? kv + row_off[i] + s * 128 + c * 16 : kv;
-                        cp_async_16_zfill(dst, src, use_row ? 16u : 0u);
-                    }
+                if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(ngw * nslabs * 4 * 128));
+                __syncwarp();
+                if (lane < ngw) {
+                    for (int hs = 0; hs < nslabs; ++hs)
+                        tma_gather4(dst_base + hs * kSlabBytes + k * 512, &kv_map, full, (slab0 + hs) * 64, y[0], y[1],
+                                    y[2], y[3], pol_kv);
                 }
-                cp_async_arrive_noinc(full);
             }
         }
         if (stop && lane == 0) {
             atomicOr(p.err, kErrWaitTimeout);
             ctl.abort = 1;
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
-        if (warp == 0 && lane == 0 && nblk > 0) {         // nor the q load
+        if (lane == 0 && ctl.abort) {  // no gather this warp issued outlives the CTA (bounded waits)
+            for (int pos = last_v; pos >= 0 && pos > last_v - kVRing; --pos)
+                wait_landed_m(&ctl.v_full[pos & (kVRing - 1)], uint32_t(pos / kVRing) & 1u);
+            for (int n = last_r; n >= 0 && n > last_r - kRRing; --n)
+                wait_landed_m(&ctl.r_full[n & (kRRing - 1)], uint32_t(n / kRRing) & 1u);
+        }
+        if (warp == 0 && lane == 0 && nblk > 0) {  // nor the q load
             const uint32_t addr = smem_u32(&ctl.q_full);
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(addr, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
@@ -349,7 +374,6 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                         stop = true;
                         break;
                     }
-                    fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
                     tc_fence_after_sync();
 #pragma unroll
                     for (int hs = 0; hs < 2; ++hs) {
@@ -370,7 +394,6 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                         stop = true;
                         break;
                     }
-                    fence_proxy_async_smem();
                     tc_fence_after_sync();
                     const uint64_t a = smem_desc_kmajor_sw128(q_addr + 8 * kSlabBytes);
                     const uint64_t bd = smem_desc_kmajor_sw128(s_base + kOffR + slot * kSlabBytes);
@@ -590,7 +613,7 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(const MlaParams p) {
 
 size_t mla_smem_bytes() { return size_t(kSmemM); }
 
-cudaError_t launch_mla(const CUtensorMap& q_map, const MlaParams& p, cudaStream_t stream) {
+cudaError_t launch_mla(const CUtensorMap& q_map, const CUtensorMap& kv_map, const MlaParams& p, cudaStream_t stream) {
     static SmemLimitOnce smem_limit;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -608,7 +631,7 @@ cudaError_t launch_mla(const CUtensorMap& q_map, const MlaParams& p, cudaStream_
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, q_map, p);
+    e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, q_map, kv_map, p);
     if (e != cudaSuccess || p.splits == 1) return e;
     cfg.gridDim = dim3(kMlaHeads / 8, unsigned(p.batch));
     cfg.blockDim = dim3(256);

@@ -25,15 +25,26 @@ __device__ __forceinline__ int pack_meta(int b, int pair, bool ok0, bool ok1) {
 __device__ __forceinline__ int meta_row(int m) { return m >> 17; }
 __device__ __forceinline__ int meta_pair(int m) { return (m >> 2) & 0x7FFF; }
 
-// Live C4 count and first work unit of every request (in shared memory).
+// Live C4 count and first work unit of every request: two arrays in shared
+// memory, sized by the launch's batch (placed after a kernel's fixed layout).
 struct RowTable {
-    int32_t n_live[kMaxBatch];
-    int32_t unit_start[kMaxBatch + 1];
+    int32_t* n_live;      // [batch]
+    int32_t* unit_start;  // [batch + 1]
 };
+
+// Shared-memory bytes of the table for `batch` requests (a 16-byte multiple).
+__host__ __device__ constexpr size_t row_table_bytes(int batch) {
+    return (size_t(2 * batch + 1) * sizeof(int32_t) + 15) & ~size_t(15);
+}
+
+__device__ __forceinline__ RowTable row_table_at(uint8_t* base, int batch) {
+    int32_t* a = reinterpret_cast<int32_t*>(base);
+    return RowTable{a, a + batch};
+}
 
 // One warp fills the table: n_b = ceil(clamp(seq_len_b, 0, max_context) / 4), units of
 // kUnitPositions positions, exclusive prefix of units.  Flags clamped lengths (CTA 0).
-__device__ __forceinline__ void build_row_table(RowTable& t, const ScoresParams& p, int lane) {
+__device__ __forceinline__ void build_row_table(const RowTable& t, const ScoresParams& p, int lane) {
     const int batch = p.batch;
     const int per = (batch + 31) / 32;  // lane l owns rows [l*per, (l+1)*per)
     const int b0 = min(lane * per, batch), b1 = min(b0 + per, batch);
@@ -142,29 +153,11 @@ struct UnitSchedule {
 };
 
 // Stream -inf over every row's positions past its request's live units (all
-// `tokens` rows of a request share the extent), rows split over all CTAs
-// (threads et in [0, nthreads) of each CTA take part).
-__device__ __forceinline__ void fill_dead_tails(const RowTable& t, const ScoresParams& p, int et, int nthreads,
-                                                int tokens = 1) {
-    const int64_t M = p.row_width;
-    const float neg_inf = __int_as_float(0xff800000);
-    const float4 ninf4 = make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
-    const int64_t stride = int64_t(gridDim.x) * nthreads;
-    for (int b = 0; b < p.batch; ++b) {
-        const int64_t units = t.unit_start[b + 1] - t.unit_start[b];
-        const int64_t extent = units * kUnitPositions < M ? units * kUnitPositions : M;
-        for (int j = 0; j < tokens; ++j) {
-            float4* row = reinterpret_cast<float4*>(p.out + (int64_t(b) * tokens + j) * M);
-            for (int64_t i = extent / 4 + int64_t(blockIdx.x) * nthreads + et; i < M / 4; i += stride)
-                __stcs(row + i, ninf4);
-        }
-    }
-}
-
-// The same -inf fill done by one warp per CTA (lane = `lane`), off the
-// epilogue's path: the dead float4s of all rows, taken in row order as one
-// flat range, are split into equal contiguous shares, one per CTA, and each
-// share is written by the warp with consecutive lanes on consecutive float4s.
+// `tokens` rows of a request share the extent), done by one warp per CTA
+// (lane = `lane`) beside the pipeline: the dead float4s of all rows, taken in
+// row order as one flat range, are split into equal contiguous shares, one per
+// CTA, and each share is written by the warp with consecutive lanes on
+// consecutive float4s.
 __device__ __forceinline__ void fill_dead_tails_warp(const RowTable& t, const ScoresParams& p, int lane,
                                                      int tokens = 1) {
     const int64_t M4 = p.row_width / 4;

@@ -46,8 +46,8 @@
 //     per unit (hi then lo, two K-slices each), into one of 4 TMEM
 //     accumulators of 32 columns.
 //   * warps 4-7: tcgen05.ld, relu, weighted head sum, key scale, live mask,
-//     128-byte stores; first the -inf fill of the dead tail of every row when
-//     a full row is requested.
+//     128-byte stores.  The -inf fill of the rows' dead parts (full-width
+//     rows) is the splitter's, after its first split.
 //   * Every wait is bounded (about 1 s); a timeout sets an error bit, stops
 //     all roles, drains in-flight copies and MMAs and frees TMEM.
 #include <cuda.h>
@@ -67,12 +67,14 @@ using namespace scores;
 
 // Three CTAs per SM, two TMA-issuing producer warps each: one issuing thread
 // keeps too few 4 KiB boxes in flight to cover HBM latency (a TMA instruction
-// takes about 120 cycles to issue), so each SM runs six issuers.
-constexpr int kStages = 5;       // key-code stages of 8 KiB (two pages), shared by the producer warps
+// takes about 120 cycles to issue), so each SM runs six issuers.  The kernel
+// is a template on its number S of 8 KiB key-code stages (two pages each,
+// shared by the producer warps); five are used (four and six measured the
+// same).
 constexpr int kQRaw = 2;         // staged bf16 query rows
 constexpr int kQSlots = 2;       // split e4m3 query tiles
 constexpr int kAccStages = 4;
-constexpr int kRing = 16;        // metadata and scale ring, >= kStages + kAccStages + 1 (a power of two)
+constexpr int kRing = 16;        // metadata and scale ring, >= S + kAccStages + 1 (a power of two)
 constexpr int kCtasPerSm = 3;
 constexpr int kAccCols = 32;     // N = 32 heads
 constexpr uint32_t kTmemCols = kAccStages * kAccCols;  // 128
@@ -86,12 +88,12 @@ constexpr int kUnitScaleBytes = 2 * kPageScaleBytes;       // 512 B
 constexpr int kWRowBytes = kHeads * 4;                     // 128 B
 constexpr uint32_t kFullArrivals = 1 + 32;                 // producer lane 0 + its 32 lanes' scale copies
 constexpr uint32_t kIdesc = idesc_e4m3_f32(128, kAccCols);
-static_assert(kRing >= kStages + kAccStages + 1, "metadata ring too small");
 static_assert(kTmemCols * kCtasPerSm <= 512, "TMEM columns per SM");
 
+template <int S>
 struct __align__(16) SmemCtl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[S];
+    uint64_t empty[S];
     uint64_t qraw_full[kQRaw];
     uint64_t qraw_empty[kQRaw];
     uint64_t q8_full[kQSlots];
@@ -105,18 +107,25 @@ struct __align__(16) SmemCtl {
     int32_t meta[kRing];
     int32_t qrow[kQRaw];                      // request of each staged query (-1: no more)
     __align__(16) float wq[kQSlots][kHeads];  // w_h * S_h of each split query
-    RowTable rows;
 };
 
-// Tile region (1024-byte aligned base): stages | q8 slots | raw queries | scales | raw weights.
-constexpr size_t kOffQ8 = size_t(kStages) * kStageBytes;
-constexpr size_t kOffQRaw = kOffQ8 + size_t(kQSlots) * kQ8Bytes;
-constexpr size_t kOffScales = kOffQRaw + size_t(kQRaw) * kQRowBytes;
-constexpr size_t kOffWRaw = kOffScales + size_t(kRing) * kUnitScaleBytes;
-constexpr size_t kTileBytes = kOffWRaw + size_t(kQRaw) * kWRowBytes;
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes + sizeof(SmemCtl);
-static_assert(kTileBytes % 16 == 0, "control block alignment");
-static_assert(kSmemBytes * kCtasPerSm <= 226 * 1024, "shared memory budget per SM");
+// Shared memory: the tile region (1024-byte aligned base: stages | q8 slots |
+// raw queries | scales | raw weights), the control block, the row table.
+template <int S>
+struct Fp8Layout {
+    static_assert(kRing >= S + kAccStages + 1, "metadata ring too small");
+    static constexpr size_t kOffQ8 = size_t(S) * kStageBytes;
+    static constexpr size_t kOffQRaw = kOffQ8 + size_t(kQSlots) * kQ8Bytes;
+    static constexpr size_t kOffScales = kOffQRaw + size_t(kQRaw) * kQRowBytes;
+    static constexpr size_t kOffWRaw = kOffScales + size_t(kRing) * kUnitScaleBytes;
+    static constexpr size_t kTileBytes = kOffWRaw + size_t(kQRaw) * kWRowBytes;
+    static_assert(kTileBytes % 16 == 0, "control block alignment");
+    static constexpr size_t kFixedBytes = 1024 /* alignment slack */ + kTileBytes + sizeof(SmemCtl<S>);
+    static constexpr size_t bytes(int batch) { return kFixedBytes + row_table_bytes(batch); }
+    static constexpr bool fits(int batch) { return bytes(batch) * kCtasPerSm <= 226 * 1024; }
+};
+constexpr int kFp8Stages = 5;
+static_assert(Fp8Layout<kFp8Stages>::fits(kMaxBatch), "shared memory budget per SM");
 
 // 16-byte global -> shared copy through L2 only (cp.async), and the arrival on
 // `bar` that fires once all of this thread's earlier cp.async copies landed
@@ -155,16 +164,22 @@ __device__ __forceinline__ void split8(const float* x, uint2& hi, uint2& lo) {
     lo = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
 }
 
+template <int S>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     scores_fp8_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap qraw_map,
                       const __grid_constant__ CUtensorMap w_map, const ScoresParams p) {
+    constexpr int kStages = S;
+    constexpr size_t kOffQ8 = Fp8Layout<S>::kOffQ8, kOffQRaw = Fp8Layout<S>::kOffQRaw;
+    constexpr size_t kOffScales = Fp8Layout<S>::kOffScales, kOffWRaw = Fp8Layout<S>::kOffWRaw;
+    constexpr size_t kTileBytes = Fp8Layout<S>::kTileBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* q8 = tiles + kOffQ8;
     uint8_t* qraw = tiles + kOffQRaw;
     const float* scale_ring = reinterpret_cast<const float*>(tiles + kOffScales);
     const float* wraw = reinterpret_cast<const float*>(tiles + kOffWRaw);
-    SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(tiles + kTileBytes);
+    SmemCtl<S>& ctl = *reinterpret_cast<SmemCtl<S>*>(tiles + kTileBytes);
+    const RowTable rows = row_table_at(tiles + kTileBytes + sizeof(SmemCtl<S>), p.batch);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -202,12 +217,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     pdl_wait_prior_grid();
     pdl_allow_next_grid();
-    if (warp == 1) build_row_table(ctl.rows, p, lane);
+    if (warp == 1) build_row_table(rows, p, lane);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
 
-    const int total_units = ctl.rows.unit_start[batch];
+    const int total_units = rows.unit_start[batch];
     const uint32_t tmem_base = ctl.tmem_base;
     const int64_t M = p.row_width;
 
@@ -230,11 +245,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         UnitSchedule sched(total_units);
         int cur_u0, cur_cnt;
         sched.next(cur_u0, cur_cnt);
-        UnitPrep cur = prepare_units(ctl.rows, p, cur_u0, cur_cnt, lane);
+        UnitPrep cur = prepare_units(rows, p, cur_u0, cur_cnt, lane);
         while (cur_cnt > 0 && !stop) {
             int nxt_u0, nxt_cnt;
             sched.next(nxt_u0, nxt_cnt);
-            const UnitPrep nxt = prepare_units(ctl.rows, p, nxt_u0, nxt_cnt, lane);  // loads in flight
+            const UnitPrep nxt = prepare_units(rows, p, nxt_u0, nxt_cnt, lane);  // loads in flight
             for (int i = 0; i < cur_cnt; ++i, ++seq) {
                 const int bi = __shfl_sync(0xffffffffu, cur.b, i);
                 const bool new_row = bi != prev_b;
@@ -411,8 +426,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         __syncwarp();
     } else if (warp == 2) {
         // ================= query splitter: bf16 q -> hi/lo e4m3 tile and w_h * S_h =================
+        // After the first split (the first MMA waits for it) this warp also streams the CTA's
+        // share of the -inf fill of the rows' dead parts when a full-width row is requested.
         const int h = lane;  // head
-        bool stop = false;
+        bool stop = false, filled = !p.fill_dead;
         for (int j = 0;; ++j) {
             const int rs = j % kQRaw;
             if (!mbar_wait(&ctl.qraw_full[rs], (j / kQRaw) & 1, &ctl.abort)) {
@@ -466,17 +483,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             mbar_arrive(&ctl.qraw_empty[rs]);
             fence_proxy_async_smem();
             mbar_arrive(&ctl.q8_full[qs]);
+            if (!filled) {
+                fill_dead_tails_warp(rows, p, lane);
+                filled = true;
+            }
         }
+        if (!filled && !stop) fill_dead_tails_warp(rows, p, lane);  // a CTA without units
         if (stop && lane == 0) {
             atomicOr(p.err, kErrWaitTimeout);
             ctl.abort = 1;
         }
     } else if (warp >= 4) {
         // ================= epilogue: warps 4..7 =================
-        const int et = threadIdx.x - 128;  // 0..127
         const int quad = warp & 3;         // TMEM lanes [32*quad, 32*quad + 32)
         const float neg_inf = __int_as_float(0xff800000);
-        if (p.fill_dead) fill_dead_tails(ctl.rows, p, et, kEpiThreads);
 
         int cur_b = -1, n = 0, q_used = -1;
         const float* wv = ctl.wq[0];  // w_h * S_h of the current request (shared memory)
@@ -498,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (q_used >= 0 && lane == 0) mbar_arrive(&ctl.q8_empty[q_used % kQSlots]);  // done with that query
                 ++q_used;
                 wv = ctl.wq[q_used % kQSlots];
-                n = ctl.rows.n_live[b];
+                n = rows.n_live[b];
                 cur_b = b;
             }
             if (!__all_sync(0xffffffffu, mbar_wait(&ctl.tfull[acc], acc_phase, &ctl.abort))) {
@@ -542,15 +562,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 }
 
-}  // namespace
-
-cudaError_t launch_scores_fp8(const CUtensorMap& codes_map, const CUtensorMap& qraw_map, const CUtensorMap& w_map,
-                              const ScoresParams& p, cudaStream_t stream) {
-    static SmemLimitOnce smem_limit;
+template <int S>
+cudaError_t launch_scores_fp8_s(const CUtensorMap& codes_map, const CUtensorMap& qraw_map, const CUtensorMap& w_map,
+                                const ScoresParams& p, cudaStream_t stream) {
+    static SmemLimitOnce smem_limit;  // the dynamic shared-memory limit, enough for any batch
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = smem_limit.apply(dev, scores_fp8_kernel, int(kSmemBytes));
+    e = smem_limit.apply(dev, scores_fp8_kernel<S>, int(Fp8Layout<S>::bytes(kMaxBatch)));
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -558,14 +577,21 @@ cudaError_t launch_scores_fp8(const CUtensorMap& codes_map, const CUtensorMap& q
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(sms * kCtasPerSm));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = Fp8Layout<S>::bytes(p.batch);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, scores_fp8_kernel, codes_map, qraw_map, w_map, p);
+    return cudaLaunchKernelEx(&cfg, scores_fp8_kernel<S>, codes_map, qraw_map, w_map, p);
+}
+
+}  // namespace
+
+cudaError_t launch_scores_fp8(const CUtensorMap& codes_map, const CUtensorMap& qraw_map, const CUtensorMap& w_map,
+                              const ScoresParams& p, cudaStream_t stream) {
+    return launch_scores_fp8_s<kFp8Stages>(codes_map, qraw_map, w_map, p, stream);
 }
 
 }  // namespace dsa

@@ -65,15 +65,17 @@ namespace {
 
 using namespace scores;
 
-// Per query-token count Q.  Q = 1: three CTAs per SM, two TMA-issuing
-// producer warps each: one issuing thread keeps too few page boxes in flight
-// to cover HBM latency (a TMA instruction takes about 120 cycles to issue),
-// so each SM runs six issuers.  Q >= 2: the Q x 4 KiB query tiles and the
-// 32 Q-column accumulators need two CTAs per SM.
-template <int Q>
+// Per query-token count Q and stage count S.  Q = 1: three CTAs per SM, two
+// TMA-issuing producer warps each: one issuing thread keeps too few page
+// boxes in flight to cover HBM latency (a TMA instruction takes about 120
+// cycles to issue), so each SM runs six issuers, with three stages each (four
+// measured the same: at this depth the ring is not the limit).  Q >= 2: the
+// Q x 4 KiB query tiles and the 32 Q-column accumulators need two CTAs per SM
+// (four stages).
+template <int Q, int S>
 struct Cfg {
     static constexpr int kCtasPerSm = Q == 1 ? 3 : 2;
-    static constexpr int kStages = Q == 1 ? 3 : 4;           // 16 KiB stages per CTA, shared by the producers
+    static constexpr int kStages = S;                         // 16 KiB stages per CTA, shared by the producers
     static constexpr int kEpiGroups = Q >= 3 ? 2 : 1;         // epilogue groups of 4 warps (Q >= 3: Q passes per unit)
     static constexpr int kQSlots = 2;
     static constexpr int kAccStages = Q <= 2 ? 4 : 2;
@@ -92,44 +94,51 @@ struct Cfg {
     static_assert(int(kTmemCols) * kCtasPerSm <= 512, "TMEM columns per SM");
 };
 
-template <int Q>
+template <int Q, int S>
 struct __align__(16) SmemCtl {
-    uint64_t full[Cfg<Q>::kStages];
-    uint64_t empty[Cfg<Q>::kStages];
-    uint64_t qfull[Cfg<Q>::kQSlots];
-    uint64_t qempty[Cfg<Q>::kQSlots];
-    uint64_t tfull[Cfg<Q>::kAccStages];
-    uint64_t tempty[Cfg<Q>::kAccStages];
-    uint64_t tmeta[Cfg<Q>::kAccStages];
+    uint64_t full[Cfg<Q, S>::kStages];
+    uint64_t empty[Cfg<Q, S>::kStages];
+    uint64_t qfull[Cfg<Q, S>::kQSlots];
+    uint64_t qempty[Cfg<Q, S>::kQSlots];
+    uint64_t tfull[Cfg<Q, S>::kAccStages];
+    uint64_t tempty[Cfg<Q, S>::kAccStages];
+    uint64_t tmeta[Cfg<Q, S>::kAccStages];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    int32_t meta[Cfg<Q>::kMetaRing];
-    __align__(16) float wtok[4 * Cfg<Q>::kEpiGroups][Q > 1 ? Q : 1][kHeads];  // Q > 1: each epilogue warp's copy of the head weights
-    RowTable rows;
+    int32_t meta[Cfg<Q, S>::kMetaRing];
+    __align__(16) float wtok[4 * Cfg<Q, S>::kEpiGroups][Q > 1 ? Q : 1][kHeads];  // Q > 1: each epilogue warp's copy of the head weights
 };
 
-template <int Q>
+// Shared memory: 1024-byte aligned tiles (stages, query slots), the control
+// block, then the batch-sized row table.
+template <int Q, int S>
 struct Layout {
     static constexpr size_t kTileBytes =
-        size_t(Cfg<Q>::kStages) * Cfg<Q>::kStageBytes + size_t(Cfg<Q>::kQSlots) * Cfg<Q>::kQTileBytes;
-    static constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kTileBytes + sizeof(SmemCtl<Q>);
-    static_assert(kSmemBytes * Cfg<Q>::kCtasPerSm <= 226 * 1024, "shared memory budget per SM");
+        size_t(Cfg<Q, S>::kStages) * Cfg<Q, S>::kStageBytes + size_t(Cfg<Q, S>::kQSlots) * Cfg<Q, S>::kQTileBytes;
+    static constexpr size_t kFixedBytes = 1024 /* alignment slack */ + kTileBytes + sizeof(SmemCtl<Q, S>);
+    static constexpr size_t bytes(int batch) { return kFixedBytes + row_table_bytes(batch); }
+    // Whether kCtasPerSm CTAs fit one SM's shared memory for this batch.
+    static constexpr bool fits(int batch) { return bytes(batch) * Cfg<Q, S>::kCtasPerSm <= 226 * 1024; }
 };
+static_assert(Layout<1, 3>::fits(kMaxBatch) && Layout<2, 4>::fits(kMaxBatch) && Layout<3, 4>::fits(kMaxBatch) &&
+                  Layout<4, 4>::fits(kMaxBatch),
+              "shared memory budget per SM");
 
-template <int Q>
-__global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
+template <int Q, int S>
+__global__ void __launch_bounds__(Cfg<Q, S>::kThreads, Cfg<Q, S>::kCtasPerSm)
     scores_kernel(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CUtensorMap q_map,
                   const ScoresParams p) {
-    using C = Cfg<Q>;
+    using C = Cfg<Q, S>;
     constexpr int kStages = C::kStages, kEpiGroups = C::kEpiGroups, kQSlots = C::kQSlots;
     constexpr int kAccStages = C::kAccStages, kMetaRing = C::kMetaRing, kAccCols = C::kAccCols;
-    constexpr int kEpiThreads = C::kEpiThreads, kStageBytes = C::kStageBytes, kQTileBytes = C::kQTileBytes;
+    constexpr int kStageBytes = C::kStageBytes, kQTileBytes = C::kQTileBytes;
     constexpr uint32_t kTmemCols = C::kTmemCols, kIdesc = C::kIdesc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* qtiles = tiles + size_t(kStages) * kStageBytes;
-    SmemCtl<Q>& ctl = *reinterpret_cast<SmemCtl<Q>*>(tiles + Layout<Q>::kTileBytes);
+    SmemCtl<Q, S>& ctl = *reinterpret_cast<SmemCtl<Q, S>*>(tiles + Layout<Q, S>::kTileBytes);
+    const RowTable rows = row_table_at(tiles + Layout<Q, S>::kTileBytes + sizeof(SmemCtl<Q, S>), p.batch);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -164,18 +173,18 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
     pdl_allow_next_grid();
 
     // ---- per-row live counts and unit prefix.
-    if (warp == 3) build_row_table(ctl.rows, p, lane);
+    if (warp == 3) build_row_table(rows, p, lane);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
 
-    const int total_units = ctl.rows.unit_start[batch];
+    const int total_units = rows.unit_start[batch];
     const uint32_t tmem_base = ctl.tmem_base;
     const int64_t M = p.row_width;
 
     if (warp == 3) {
         // ================= set-up warp, then the -inf fill of the rows' dead parts (full-width rows) =================
-        if (p.fill_dead) fill_dead_tails_warp(ctl.rows, p, lane, Q);
+        if (p.fill_dead) fill_dead_tails_warp(rows, p, lane, Q);
     } else if (warp == 0 || warp == 2) {
         // ================= producers: warp 0 issues the CTA's even units, warp 2 the odd ones =================
         // Both walk the same unit sequence (page ids fetched one batch ahead); a row change is
@@ -194,11 +203,11 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
         UnitSchedule sched(total_units);
         int cur_u0, cur_cnt;
         sched.next(cur_u0, cur_cnt);
-        UnitPrep cur = prepare_units(ctl.rows, p, cur_u0, cur_cnt, lane);
+        UnitPrep cur = prepare_units(rows, p, cur_u0, cur_cnt, lane);
         while (cur_cnt > 0 && !stop) {
             int nxt_u0, nxt_cnt;
             sched.next(nxt_u0, nxt_cnt);
-            const UnitPrep nxt = prepare_units(ctl.rows, p, nxt_u0, nxt_cnt, lane);  // loads in flight
+            const UnitPrep nxt = prepare_units(rows, p, nxt_u0, nxt_cnt, lane);  // loads in flight
             for (int i = 0; i < cur_cnt; ++i, ++seq) {
                 const int bi = __shfl_sync(0xffffffffu, cur.b, i);
                 const bool new_row = bi != prev_b;
@@ -348,7 +357,6 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
         __syncwarp();
     } else if (warp >= 4) {
         // ================= epilogue: kEpiGroups groups of 4 warps =================
-        const int et = threadIdx.x - 128;   // 0 .. kEpiThreads-1
         const int group = (warp - 4) >> 2;  // takes the group-th, (group + kEpiGroups)-th, ... units
         const int quad = warp & 3;          // TMEM lanes [32*quad, 32*quad + 32)
         const float neg_inf = __int_as_float(0xff800000);
@@ -385,7 +393,7 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
                         wv[4 * h4 + 2] = v.z;
                         wv[4 * h4 + 3] = v.w;
                     }
-                    n_tok[0] = ctl.rows.n_live[b];
+                    n_tok[0] = rows.n_live[b];
                 } else {  // this warp's copy of the Q x 32 head weights; per-token causal lengths
                     __syncwarp();
 #pragma unroll
@@ -399,7 +407,7 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
                         n_tok[j] = Lj > 0 ? int((Lj + 3) >> 2) : 0;
                     }
                 }
-                n = ctl.rows.n_live[b];
+                n = rows.n_live[b];
                 cur_b = b;
             }
             const bool okf = mbar_wait(&ctl.tfull[acc], acc_phase, &ctl.abort);
@@ -466,29 +474,29 @@ __global__ void __launch_bounds__(Cfg<Q>::kThreads, Cfg<Q>::kCtasPerSm)
     }
 }
 
-template <int Q>
+template <int Q, int S>
 cudaError_t launch_scores_q(const CUtensorMap& keys_map, const CUtensorMap& q_map, const ScoresParams& p,
                             cudaStream_t stream) {
-    static SmemLimitOnce smem_limit;
+    static SmemLimitOnce smem_limit;  // the dynamic shared-memory limit, enough for any batch
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = smem_limit.apply(dev, scores_kernel<Q>, int(Layout<Q>::kSmemBytes));
+    e = smem_limit.apply(dev, scores_kernel<Q, S>, int(Layout<Q, S>::bytes(kMaxBatch)));
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(sms * Cfg<Q>::kCtasPerSm));
-    cfg.blockDim = dim3(Cfg<Q>::kThreads);
-    cfg.dynamicSmemBytes = Layout<Q>::kSmemBytes;
+    cfg.gridDim = dim3(unsigned(sms * Cfg<Q, S>::kCtasPerSm));
+    cfg.blockDim = dim3(Cfg<Q, S>::kThreads);
+    cfg.dynamicSmemBytes = Layout<Q, S>::bytes(p.batch);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, scores_kernel<Q>, keys_map, q_map, p);
+    return cudaLaunchKernelEx(&cfg, scores_kernel<Q, S>, keys_map, q_map, p);
 }
 
 }  // namespace
@@ -496,10 +504,10 @@ cudaError_t launch_scores_q(const CUtensorMap& keys_map, const CUtensorMap& q_ma
 cudaError_t launch_scores(const CUtensorMap& keys_map, const CUtensorMap& q_map, const ScoresParams& p,
                           cudaStream_t stream) {
     switch (p.tokens) {
-        case 1: return launch_scores_q<1>(keys_map, q_map, p, stream);
-        case 2: return launch_scores_q<2>(keys_map, q_map, p, stream);
-        case 3: return launch_scores_q<3>(keys_map, q_map, p, stream);
-        case 4: return launch_scores_q<4>(keys_map, q_map, p, stream);
+        case 1: return launch_scores_q<1, 3>(keys_map, q_map, p, stream);
+        case 2: return launch_scores_q<2, 4>(keys_map, q_map, p, stream);
+        case 3: return launch_scores_q<3, 4>(keys_map, q_map, p, stream);
+        case 4: return launch_scores_q<4, 4>(keys_map, q_map, p, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -197,3 +197,28 @@ def test_mla_workspace_reused(gpu_lib, oracle):
     for (o, lse), mc in zip(outs, (mc1, mc2, mc1)):
         of, lf = _run(b, mc)
         assert np.array_equal(o, of) and np.array_equal(lse, lf)
+
+
+def test_mla_bad_page_ids(gpu_lib, oracle):
+    """A live page id outside [0, num_pages) sets the bad-page bit and is never read: requests
+    whose pages are all valid still match the oracle, on the same call (the row gathers take
+    another row of the request in place of the bad entry, so nothing outside the cache is read)."""
+    import torch
+    from sparse_attention_paged_dsa_gb300 import binding as b
+    mc = I.mla_case(I.workload("b16_ctx8k_mixed"))
+    table = mc.page_table.copy()
+    n_pages = mc.kv.shape[0]
+    bad_rows = [3, 7]
+    for r in bad_rows:   # the first page of these requests (their top-k rows use it): out of range, then negative
+        n = (int(mc.seq_lens[r]) + 3) // 4
+        assert ((mc.topk[r] >= 0) & (mc.topk[r] < min(64, n))).any()
+    for r in bad_rows:
+        table[r, 0] = n_pages + 5 if r == 3 else -7
+    q, kv, _, seq, topk = _dev(mc)
+    t = torch.from_numpy(table).cuda()
+    ws = torch.zeros(b.sparse_mla_workspace_size(mc.batch, mc.topk.shape[1]), dtype=torch.uint8, device="cuda")
+    o, lse = b.dsa_sparse_mla_decode(q, kv, t, seq, mc.max_context, topk, mc.sm_scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert b.get_error(ws) & 0x2, "bad-page bit not set"
+    good = [r for r in range(mc.batch) if r not in bad_rows]
+    _check(o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), mc, oracle, rows=good)
