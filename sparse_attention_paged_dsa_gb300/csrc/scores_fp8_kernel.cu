@@ -497,6 +497,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // ================= epilogue: warps 4..7 =================
         const int quad = warp & 3;         // TMEM lanes [32*quad, 32*quad + 32)
         const float neg_inf = __int_as_float(0xff800000);
+        // The scores stay in L2 for the top-k that reads them next (the keys stream through
+        // it evict-first); without the hint about two thirds of a dense 128K step's 8 MB of
+        // scores were written back to HBM before the top-k read them.
+        const uint64_t pol_row = l2_policy_evict_last();
 
         int cur_b = -1, n = 0, q_used = -1;
         const float* wv = ctl.wq[0];  // w_h * S_h of the current request (shared memory)
@@ -538,15 +542,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                 for (int h4 = 0; h4 < kHeads / 4; ++h4) {
                     const float4 wq = w4[h4];
-                    s0 = fmaf(wq.x, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f), s0);
-                    s1 = fmaf(wq.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), s1);
-                    s2 = fmaf(wq.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), s2);
-                    s3 = fmaf(wq.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), s3);
+                    fma2(s0, s1, wq.x, wq.y, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f),
+                         fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f));
+                    fma2(s2, s3, wq.z, wq.w, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f),
+                         fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f));
                 }
             }
             const float s = key_scale * ((s0 + s1) + (s2 + s3));
             const int64_t t = int64_t(pair) * kUnitPositions + quad * 32 + lane;
-            if (t < M) p.out[int64_t(b) * M + t] = (t < n && page_ok) ? s : neg_inf;
+            if (t < M) st_global_hint(p.out + int64_t(b) * M + t, (t < n && page_ok) ? s : neg_inf, pol_row);
         }
         if (stop && lane == 0) {
             atomicOr(p.err, kErrWaitTimeout);

@@ -360,6 +360,10 @@ __global__ void __launch_bounds__(Cfg<Q, S>::kThreads, Cfg<Q, S>::kCtasPerSm)
         const int group = (warp - 4) >> 2;  // takes the group-th, (group + kEpiGroups)-th, ... units
         const int quad = warp & 3;          // TMEM lanes [32*quad, 32*quad + 32)
         const float neg_inf = __int_as_float(0xff800000);
+        // The scores stay in L2 for the top-k that reads them next (the keys stream through
+        // it evict-first); without the hint about two thirds of a dense 128K step's 8 MB of
+        // scores were written back to HBM before the top-k read them.
+        const uint64_t pol_row = l2_policy_evict_last();
 
 
         int cur_b = -1, n = 0;
@@ -425,16 +429,16 @@ __global__ void __launch_bounds__(Cfg<Q, S>::kThreads, Cfg<Q, S>::kCtasPerSm)
                 tc_fence_before_sync();
                 mbar_arrive(&ctl.tempty[acc]);
 
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // heads h = 0, 1, 2, 3 mod 4
 #pragma unroll
                 for (int h = 0; h < kHeads; h += 4) {
-                    s0 = fmaf(wv[h + 0], fmaxf(__uint_as_float(r[h + 0]), 0.f), s0);
-                    s1 = fmaf(wv[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), s1);
-                    s2 = fmaf(wv[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.f), s2);
-                    s3 = fmaf(wv[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.f), s3);
+                    fma2(s0, s1, wv[h + 0], wv[h + 1], fmaxf(__uint_as_float(r[h + 0]), 0.f),
+                         fmaxf(__uint_as_float(r[h + 1]), 0.f));
+                    fma2(s2, s3, wv[h + 2], wv[h + 3], fmaxf(__uint_as_float(r[h + 2]), 0.f),
+                         fmaxf(__uint_as_float(r[h + 3]), 0.f));
                 }
                 const float s = (s0 + s1) + (s2 + s3);
-                if (t < M) p.out[int64_t(b) * M + t] = (t < n && page_ok) ? s : neg_inf;
+                if (t < M) st_global_hint(p.out + int64_t(b) * M + t, (t < n && page_ok) ? s : neg_inf, pol_row);
             } else {
 #pragma unroll 1
                 for (int j = 0; j < Q; ++j) {  // token j: accumulator columns [32 j, 32 j + 32)
@@ -446,17 +450,19 @@ __global__ void __launch_bounds__(Cfg<Q, S>::kThreads, Cfg<Q, S>::kCtasPerSm)
                         mbar_arrive(&ctl.tempty[acc]);
                     }
                     const float4* wr = reinterpret_cast<const float4*>(ctl.wtok[warp - 4][j]);
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // heads h = 0, 1, 2, 3 mod 4
 #pragma unroll
                     for (int h4 = 0; h4 < kHeads / 4; ++h4) {
                         const float4 wq = wr[h4];
-                        s0 = fmaf(wq.x, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f), s0);
-                        s1 = fmaf(wq.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), s1);
-                        s2 = fmaf(wq.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), s2);
-                        s3 = fmaf(wq.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), s3);
+                        fma2(s0, s1, wq.x, wq.y, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f),
+                             fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f));
+                        fma2(s2, s3, wq.z, wq.w, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f),
+                             fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f));
                     }
                     const float s = (s0 + s1) + (s2 + s3);
-                    if (t < M) p.out[(int64_t(b) * Q + j) * M + t] = (t < n_tok[j] && page_ok) ? s : neg_inf;
+                    if (t < M)
+                        st_global_hint(p.out + (int64_t(b) * Q + j) * M + t, (t < n_tok[j] && page_ok) ? s : neg_inf,
+                                       pol_row);
                 }
             }
         }
