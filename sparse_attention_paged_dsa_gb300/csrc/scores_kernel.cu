@@ -440,29 +440,42 @@ __global__ void __launch_bounds__(Cfg<Q, S>::kThreads, Cfg<Q, S>::kCtasPerSm)
                 const float s = (s0 + s1) + (s2 + s3);
                 if (t < M) st_global_hint(p.out + int64_t(b) * M + t, (t < n && page_ok) ? s : neg_inf, pol_row);
             } else {
-#pragma unroll 1
-                for (int j = 0; j < Q; ++j) {  // token j: accumulator columns [32 j, 32 j + 32)
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + uint32_t(32 * j), r);
-                    tmem_ld_wait(r);
-                    if (j == Q - 1) {
+                // Token j's logits are accumulator columns [32 j, 32 j + 32), read in halves of 16:
+                // the load of the next half is in flight while the current one is summed.
+                uint32_t ra[16], rb[16];
+                tmem_ld_32x32b_x16(taddr, ra);
+                tmem_ld_wait16(ra);
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // heads h = 0, 1, 2, 3 mod 4
+#pragma unroll
+                for (int hh = 0; hh < 2 * Q; ++hh) {
+                    const int j = hh >> 1;
+                    if (hh + 1 < 2 * Q) {
+                        tmem_ld_32x32b_x16(taddr + uint32_t(16 * (hh + 1)), rb);
+                    } else {  // every load from this accumulator has completed
                         tc_fence_before_sync();
                         mbar_arrive(&ctl.tempty[acc]);
                     }
-                    const float4* wr = reinterpret_cast<const float4*>(ctl.wtok[warp - 4][j]);
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // heads h = 0, 1, 2, 3 mod 4
+                    const float4* wr = reinterpret_cast<const float4*>(ctl.wtok[warp - 4][j]) + 4 * (hh & 1);
 #pragma unroll
-                    for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+                    for (int h4 = 0; h4 < 4; ++h4) {
                         const float4 wq = wr[h4];
-                        fma2(s0, s1, wq.x, wq.y, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f),
-                             fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f));
-                        fma2(s2, s3, wq.z, wq.w, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f),
-                             fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f));
+                        fma2(s0, s1, wq.x, wq.y, fmaxf(__uint_as_float(ra[4 * h4 + 0]), 0.f),
+                             fmaxf(__uint_as_float(ra[4 * h4 + 1]), 0.f));
+                        fma2(s2, s3, wq.z, wq.w, fmaxf(__uint_as_float(ra[4 * h4 + 2]), 0.f),
+                             fmaxf(__uint_as_float(ra[4 * h4 + 3]), 0.f));
                     }
-                    const float s = (s0 + s1) + (s2 + s3);
-                    if (t < M)
-                        st_global_hint(p.out + (int64_t(b) * Q + j) * M + t, (t < n_tok[j] && page_ok) ? s : neg_inf,
-                                       pol_row);
+                    if (hh & 1) {  // token j complete
+                        const float s = (s0 + s1) + (s2 + s3);
+                        if (t < M)
+                            st_global_hint(p.out + (int64_t(b) * Q + j) * M + t,
+                                           (t < n_tok[j] && page_ok) ? s : neg_inf, pol_row);
+                        s0 = s1 = s2 = s3 = 0.f;
+                    }
+                    if (hh + 1 < 2 * Q) {
+                        tmem_ld_wait16(rb);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) ra[c] = rb[c];
+                    }
                 }
             }
         }
