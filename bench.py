@@ -21,6 +21,7 @@ bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import functools
 import hashlib
 import json
 import os
@@ -348,7 +349,9 @@ def run_configs(args, binding, inputs, device, stream, main_case, main_dev):
     row, the fused call without it (live scores in the workspace), and the scores entry point alone.
     Each is timed twice: warm (20 calls captured in one CUDA graph, median of 20 replays: back to back,
     as in a decode loop) and with L2 evicted before every call (a 512 MiB read outside the events,
-    median of 30 isolated calls)."""
+    median of 30 isolated calls).  Every warm timing runs before any eviction: the keys are loaded
+    evict-first, so after a flush the flush buffer's lines would keep them out of L2 and a "warm"
+    loop that follows one is not back to back."""
     import torch
     peak, peak_kind = measured_hbm_peak()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
@@ -356,13 +359,16 @@ def run_configs(args, binding, inputs, device, stream, main_case, main_dev):
                      "30 calls, a 512 MiB read before each (outside the events), median",
            "peak_gbs": peak, "peak_kind": f"{peak_kind} (HBM copy bandwidth)"}
 
+    deferred = []  # (result dict, call): the evicted timings, run after every warm one
+    workspaces = []
+
     def time_both(fn):
         for _ in range(3):
             fn()
         torch.cuda.synchronize(device)
-        warm = graph_us_per_call(fn)
-        _, per = time_loop(fn, 30, stream, lambda: evict_l2(flush))
-        return {"warm": warm, "l2_evicted": 1e6 * statistics.median(per)}
+        res = {"warm": graph_us_per_call(fn)}
+        deferred.append((res, fn))
+        return res
 
     for name in CONFIG_WORKLOADS:
         case = main_case if name == main_case.name else inputs.workload(name)
@@ -372,24 +378,18 @@ def run_configs(args, binding, inputs, device, stream, main_case, main_dev):
         scores = torch.empty((B, M), dtype=torch.float32, device=device)
         topk = torch.empty((B, K), dtype=torch.int32, device=device)
         ws = binding.new_workspace(B, case.max_context, K, device)
-        fused_row = time_both(lambda: binding.dsa_indexer_fused(q, w, pool, table, seq, case.max_context, K,
-                                                                topk_idx=topk, scores=scores, workspace=ws))
-        fused_no_row = time_both(lambda: binding.dsa_indexer_fused(q, w, pool, table, seq, case.max_context, K,
-                                                                   topk_idx=topk, workspace=ws))
-        scores_only = time_both(lambda: binding.dsa_indexer_scores(q, w, pool, table, seq, case.max_context,
-                                                                   scores=scores, workspace=ws))
-        if binding.get_error(ws) != 0:
-            raise RuntimeError(f"device error word set in the {name} run")
+        # (partial binds this workload's tensors: the evicted timings run after the loop)
+        fused_row = time_both(functools.partial(binding.dsa_indexer_fused, q, w, pool, table, seq, case.max_context,
+                                                K, topk_idx=topk, scores=scores, workspace=ws))
+        fused_no_row = time_both(functools.partial(binding.dsa_indexer_fused, q, w, pool, table, seq,
+                                                   case.max_context, K, topk_idx=topk, workspace=ws))
+        scores_only = time_both(functools.partial(binding.dsa_indexer_scores, q, w, pool, table, seq,
+                                                  case.max_context, scores=scores, workspace=ws))
+        workspaces.append((name, ws))
         key_bytes = live * KEY_BYTES_PER_POSITION
-        gbs = lambda us: key_bytes / (us * 1e-6) / 1e9
         entry = {
             "batch": B, "max_context": case.max_context, "k": K, "live_positions": live, "live_key_bytes": key_bytes,
             "fused_row_us": fused_row, "fused_no_row_us": fused_no_row, "scores_us": scores_only,
-            "positions_per_s": {t: live / (fused_row[t] * 1e-6) for t in ("warm", "l2_evicted")},
-            "step_gbs": {t: gbs(fused_row[t]) for t in ("warm", "l2_evicted")},
-            "step_frac": {t: gbs(fused_row[t]) / peak for t in ("warm", "l2_evicted")},
-            "scores_kernel_frac": {t: gbs(scores_only[t]) / peak for t in ("warm", "l2_evicted")},
-            "fused_over_scores": {t: fused_row[t] / scores_only[t] for t in ("warm", "l2_evicted")},
             "scores_row_bytes": B * M * 4,
         }
         if name == "b64_ctx1m_seq512":
@@ -401,19 +401,36 @@ def run_configs(args, binding, inputs, device, stream, main_case, main_dev):
             q8, w8, pool8, table8, seq8 = binding.to_device(small, device)
             scores8 = torch.empty((B, 8192 // 4), dtype=torch.float32, device=device)
             ws8 = binding.new_workspace(B, 8192, K, device)
-            s8 = time_both(lambda: binding.dsa_indexer_scores(q8, w8, pool8, table8, seq8, 8192, scores=scores8,
-                                                              workspace=ws8))
+            s8 = time_both(functools.partial(binding.dsa_indexer_scores, q8, w8, pool8, table8, seq8, 8192,
+                                             scores=scores8, workspace=ws8))
+            workspaces.append((name + " at 8K width", ws8))
             entry["scores_api_fill"] = {
-                "width_1m": {"row_bytes": B * M * 4, "us": scores_only,
-                             "row_gbs": {t: B * M * 4 / (scores_only[t] * 1e-6) / 1e9 for t in scores_only}},
-                "width_8k": {"row_bytes": B * 2048 * 4, "us": s8,
-                             "row_gbs": {t: B * 2048 * 4 / (s8[t] * 1e-6) / 1e9 for t in s8}},
-                "ratio_1m_over_8k": {t: scores_only[t] / s8[t] for t in s8},
+                "width_1m": {"row_bytes": B * M * 4, "us": scores_only},
+                "width_8k": {"row_bytes": B * 2048 * 4, "us": s8},
                 "note": "the scores entry point is O(max_context) by contract (it writes the full-width row); "
                         "the O(live) bound is the fused call without a row (context_scaling)"}
-            if binding.get_error(ws8) != 0:
-                raise RuntimeError("device error word set in the 8K-width scores run")
         out[name] = entry
+    for res, fn in deferred:  # the evicted timings (the warm ones are all done)
+        _, per = time_loop(fn, 30, stream, lambda: evict_l2(flush))
+        res["l2_evicted"] = 1e6 * statistics.median(per)
+    for name, ws in workspaces:
+        if binding.get_error(ws) != 0:
+            raise RuntimeError(f"device error word set in the {name} run")
+    for name in CONFIG_WORKLOADS:  # the ratios that need both timings
+        e = out[name]
+        key_bytes = e["live_key_bytes"]
+        gbs = lambda us: key_bytes / (us * 1e-6) / 1e9
+        e["positions_per_s"] = {t: e["live_positions"] / (e["fused_row_us"][t] * 1e-6) for t in ("warm", "l2_evicted")}
+        e["step_gbs"] = {t: gbs(e["fused_row_us"][t]) for t in ("warm", "l2_evicted")}
+        e["step_frac"] = {t: gbs(e["fused_row_us"][t]) / peak for t in ("warm", "l2_evicted")}
+        e["scores_kernel_frac"] = {t: gbs(e["scores_us"][t]) / peak for t in ("warm", "l2_evicted")}
+        e["fused_over_scores"] = {t: e["fused_row_us"][t] / e["scores_us"][t] for t in ("warm", "l2_evicted")}
+        fill = e.get("scores_api_fill")
+        if fill:
+            for w in ("width_1m", "width_8k"):
+                fill[w]["row_gbs"] = {t: fill[w]["row_bytes"] / (fill[w]["us"][t] * 1e-6) / 1e9 for t in fill[w]["us"]}
+            fill["ratio_1m_over_8k"] = {t: fill["width_1m"]["us"][t] / fill["width_8k"]["us"][t]
+                                        for t in ("warm", "l2_evicted")}
     del flush
     return out
 
@@ -718,10 +735,13 @@ def run_ours(args):
     if binding.get_error(ws) != 0:
         raise RuntimeError("device error word set during the timed steps")
 
-    # e2e: host (pinned) inputs -> device, both calls, top-k back to the host, every step.
+    # e2e: the step's host (pinned) inputs -> device, both kernels, top-k back to the host, every
+    # step (key cache resident); beside it, the same with the whole key pool copied every step.
     e2e = None
     if args.e2e_steps > 0:
         e2e = run_e2e(args, case, binding, scores, topk, ws, device, stream, world, live)
+        e2e["with_key_pool_copied"] = run_e2e(args, case, binding, scores, topk, ws, device, stream, world, live,
+                                              cache_copied=True)
 
     scaling_1m = context_scaling(binding, inputs, device) if not args.no_context_scaling else None
     configs = (run_configs(args, binding, inputs, device, stream, case, (q, w, pool, table, seq))
@@ -780,21 +800,27 @@ def run_ours(args):
     return 0
 
 
-def run_e2e(args, case, binding, scores, topk, ws, device, stream, world, live):
-    """Same step through the C ABI with host buffers: H2D of every input, D2H of the top-k."""
+def run_e2e(args, case, binding, scores, topk, ws, device, stream, world, live, cache_copied=False):
+    """The same step through the C ABI with host buffers: H2D of the step's inputs from pinned memory,
+    the fused call, D2H of the top-k, all inside the timed region.  The step's inputs are the query,
+    head weights, page table and lengths; the paged key cache is the model's resident state and is
+    uploaded once before the timed region (a decode step appends one C4 key per 4 tokens per request,
+    64 B-256 B, not modelled).  With cache_copied the whole key pool is copied every step as well."""
     import torch
     import torch.distributed as dist
     B, K = case.batch, case.k
-    host = [torch.from_numpy(a).pin_memory() for a in
-            (case.q.view("int16"), case.w, case.key_pool.view("int16"), case.page_table, case.seq_lens)]
+    arrays = (case.q.view("int16"), case.w, case.key_pool.view("int16"), case.page_table, case.seq_lens)
+    host = [torch.from_numpy(a).pin_memory() for a in arrays]
     dev_in = [torch.empty(h.shape, dtype=h.dtype, device=device) for h in host]
+    per_step = [0, 1, 2, 3, 4] if cache_copied else [0, 1, 3, 4]  # index 2: the key pool
+    dev_in[2].copy_(host[2])
     out_host = torch.empty((B, K), dtype=torch.int32).pin_memory()
-    h2d = sum(h.numel() * h.element_size() for h in host)
+    h2d = sum(host[i].numel() * host[i].element_size() for i in per_step)
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
-        for d, h in zip(dev_in, host):
-            d.copy_(h, non_blocking=True)
+        for i in per_step:
+            dev_in[i].copy_(host[i], non_blocking=True)
         qd, wd, pd, td, sd = dev_in
         binding.dsa_indexer_fused(qd.view(torch.bfloat16), wd, pd.view(torch.bfloat16), td, sd,
                                   case.max_context, K, topk_idx=topk, scores=scores, workspace=ws)
@@ -815,7 +841,9 @@ def run_e2e(args, case, binding, scores, topk, ws, device, stream, world, live):
     if not np.array_equal(out_host.numpy(), topk.cpu().numpy()):
         raise RuntimeError("e2e top-k read-back mismatch")
     return {"value": e2e_units / e2e_seconds, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h,
+            "inputs": "q, w, page table, seq_lens every step" + (" and the whole key pool" if cache_copied
+                                                                 else "; key cache resident")}
 
 
 def main(argv=None):

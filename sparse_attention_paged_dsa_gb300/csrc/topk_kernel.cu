@@ -53,7 +53,8 @@ struct TopkSmem {
     uint32_t warp_gt[kWarps];
     uint32_t warp_eq[kWarps];
     uint32_t result[2];
-    uint32_t hist2[2048];                        // second histogram buffer (list pass 2)
+    uint32_t hist2[2048];                        // second histogram buffer (list pass 2; sampled path: pass 1)
+    uint32_t hist3[2048];                        // sampled path: radix pass 2
     uint32_t bits_gt[kRegCap / 32];              // sampled path: positions with key > T
     uint32_t bits_eq[kRegCap / 32];              // sampled path: positions with key == T
 };
@@ -64,7 +65,8 @@ __host__ __device__ constexpr int sampled_row_words(int n) { return (n + 3) & ~3
 
 // Find the bin holding the kk-th largest key: result[0] = bin,
 // result[1] = how many keys of that bin are still to be taken.  Ends with a
-// barrier, so result[] is visible to all threads on return.
+// barrier, so result[] is visible to all threads on return.  Every warp scans
+// the 32 warp totals itself (two barriers, no single-warp step between them).
 template <int kBins>
 __device__ __forceinline__ void select_bin_from(TopkSmem& sm, const uint32_t* hist, uint32_t kk) {
     constexpr int per = kBins / kThreads;
@@ -84,18 +86,15 @@ __device__ __forceinline__ void select_bin_from(TopkSmem& sm, const uint32_t* hi
     }
     if (lane == 0) sm.warp_tot[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-        const uint32_t t = sm.warp_tot[lane];
-        uint32_t s = t;
+    const uint32_t t = sm.warp_tot[lane];  // lane l: warp l's total
+    uint32_t sfx = t;                      // over warps l .. 31
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t x = __shfl_down_sync(0xffffffffu, s, o);
-            if (lane + o < 32) s += x;
-        }
-        sm.warp_tot[lane] = s - t;  // keys in higher warps' bins
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_down_sync(0xffffffffu, sfx, o);
+        if (lane + o < 32) sfx += x;
     }
-    __syncthreads();
-    uint32_t above = sm.warp_tot[warp] + incl - v;  // keys in bins above this thread's bins
+    const uint32_t higher = __shfl_sync(0xffffffffu, sfx - t, warp);  // keys in higher warps' bins
+    uint32_t above = higher + incl - v;  // keys in bins above this thread's bins
 #pragma unroll
     for (int i = per - 1; i >= 0; --i) {
         if (above < kk && above + h[i] >= kk) {
@@ -117,6 +116,8 @@ __device__ __forceinline__ void clear_hist(TopkSmem& sm) {
 }
 
 // Exclusive prefix over the block, in thread order, of two per-thread counts.
+// One barrier: every warp scans the 32 warp totals itself.  The totals are not
+// written again by any caller afterwards, so no barrier is needed at the end.
 __device__ __forceinline__ void block_scan2(TopkSmem& sm, uint32_t a, uint32_t b, uint32_t& a_before,
                                             uint32_t& b_before) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -135,24 +136,19 @@ __device__ __forceinline__ void block_scan2(TopkSmem& sm, uint32_t a, uint32_t b
         sm.warp_eq[warp] = bi;
     }
     __syncthreads();
-    if (warp == 0) {
-        const uint32_t g = sm.warp_gt[lane], e = sm.warp_eq[lane];
-        uint32_t gs = g, es = e;
+    const uint32_t g = sm.warp_gt[lane], e = sm.warp_eq[lane];  // lane l: warp l's totals
+    uint32_t gs = g, es = e;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t x = __shfl_up_sync(0xffffffffu, gs, o);
-            const uint32_t y = __shfl_up_sync(0xffffffffu, es, o);
-            if (lane >= o) {
-                gs += x;
-                es += y;
-            }
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, gs, o);
+        const uint32_t y = __shfl_up_sync(0xffffffffu, es, o);
+        if (lane >= o) {
+            gs += x;
+            es += y;
         }
-        sm.warp_gt[lane] = gs - g;
-        sm.warp_eq[lane] = es - e;
     }
-    __syncthreads();
-    a_before = sm.warp_gt[warp] + ai - a;
-    b_before = sm.warp_eq[warp] + bi - b;
+    a_before = __shfl_sync(0xffffffffu, gs - g, warp) + ai - a;
+    b_before = __shfl_sync(0xffffffffu, es - e, warp) + bi - b;
 }
 
 // --------------------------------------------------------------- short rows
@@ -292,11 +288,15 @@ __device__ __noinline__ void select_row_regs(TopkSmem& sm, uint32_t* stage, cons
 // more keys than the list holds pass tau -- the caller then runs the exact
 // full-row path -- and -1 when the row's copy did not land within the wait
 // limit (error bit set, the row padded with -1).
-__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(sdst)),
-                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
+// (With an L2 eviction policy: the scores kernels store the row evict-last so that it waits in L2
+// for this read; reading it evict-first hands those lines back.)
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
 }
 
 __device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, int buf_words,
@@ -320,17 +320,22 @@ __device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, i
     }
     if (tid < 4 && 4 * n4 + tid < row_words)  // the partial group: live scores, then zeros
         rs[4 * n4 + tid] = 4 * n4 + tid < n ? __ldcg(row + 4 * n4 + tid) : 0.f;
-    clear_hist(sm);
+    for (int i = tid; i < 2048; i += kThreads) {  // all three histograms: no clearing barrier later
+        sm.hist[i] = 0;
+        sm.hist2[i] = 0;
+        sm.hist3[i] = 0;
+    }
     sm.bits_gt[tid] = 0;
     sm.bits_eq[tid] = 0;
     __syncthreads();
     if (tid == 0) {
         constexpr uint32_t kChunk = 32768;
         const uint32_t bytes = uint32_t(n4) * 16u;
+        const uint64_t pol = l2_policy_evict_first();
         mbar_arrive_expect_tx(&sm.row_bar, bytes);
         for (uint32_t off = 0; off < bytes; off += kChunk)
             bulk_load(reinterpret_cast<uint8_t*>(rs) + off, reinterpret_cast<const uint8_t*>(row) + off,
-                      min(kChunk, bytes - off), &sm.row_bar);
+                      min(kChunk, bytes - off), &sm.row_bar, pol);
     }
     const bool landed = mbar_wait(&sm.row_bar, 0, &sm.abort);
     if (__syncthreads_or(!landed)) {
@@ -372,6 +377,7 @@ __device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, i
                            (live > 2 && !(v.z < f_tau) ? 4u : 0u) | (live > 3 && !(v.w < f_tau) ? 8u : 0u);
         flags |= f << (4 * j);
     }
+    clear_hist(sm);  // the sample histogram has been read (select_bin ended with a barrier)
     const uint32_t cnt = __popc(flags);
     uint32_t incl = cnt;
 #pragma unroll
@@ -396,25 +402,21 @@ __device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, i
     const int C = int(sm.ncand);
     if (C < k || C > cap) return 0;
 
-    // Exact selection on the list.  Pass 1 uses hist, pass 2 hist2 (cleared with hist), pass 3 hist again.
-    clear_hist(sm);
-    for (int i = tid; i < 2048; i += kThreads) sm.hist2[i] = 0;
+    // Exact selection on the list: pass 1 counts into hist2, pass 2 into hist3, pass 3 into hist
+    // (all three zero by now).
+    for (int i = tid; i < C; i += kThreads) atomicAdd(&sm.hist2[cand_key[i] >> 21], 1u);
     __syncthreads();
-    for (int i = tid; i < C; i += kThreads) atomicAdd(&sm.hist[cand_key[i] >> 21], 1u);
-    __syncthreads();
-    select_bin<2048>(sm, uint32_t(k));
+    select_bin_from<2048>(sm, sm.hist2, uint32_t(k));
     const uint32_t bin1 = sm.result[0];
     uint32_t kk = sm.result[1];
     for (int i = tid; i < C; i += kThreads) {
         const uint32_t ck = cand_key[i];
-        if ((ck >> 21) == bin1) atomicAdd(&sm.hist2[(ck >> 10) & 0x7FFu], 1u);
+        if ((ck >> 21) == bin1) atomicAdd(&sm.hist3[(ck >> 10) & 0x7FFu], 1u);
     }
     __syncthreads();
-    select_bin_from<2048>(sm, sm.hist2, kk);
+    select_bin_from<2048>(sm, sm.hist3, kk);
     const uint32_t prefix22 = (bin1 << 11) | sm.result[0];
     kk = sm.result[1];
-    clear_hist(sm);  // nobody reads pass 1's histogram any more
-    __syncthreads();
     for (int i = tid; i < C; i += kThreads) {
         const uint32_t ck = cand_key[i];
         if ((ck >> 10) == prefix22) atomicAdd(&sm.hist[ck & 0x3FFu], 1u);
