@@ -13,8 +13,9 @@
 // positions); every key > T and those keys == T are written in ascending
 // position.  One 1024-thread CTA per request.
 //   * n_b <= 32768, first choice (sampled path): the row is copied into shared
-//     memory by the bulk-copy engine; a histogram of every 4th key gives a
-//     threshold that keeps a little more than k keys; those are appended with
+//     memory by the bulk-copy engine; meanwhile a histogram of every 16th key,
+//     read straight from global memory, gives a threshold that keeps a little
+//     more than k keys; once the row has landed those are appended with
 //     their positions to a short list, the radix passes run on that list
 //     only, and the selected positions are marked in bitmaps whose prefix
 //     counts place each one in ascending order.
@@ -27,6 +28,7 @@
 //     compaction over per-warp segments.
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "indexer_kernels.h"
@@ -53,11 +55,13 @@ struct TopkSmem {
     uint32_t warp_gt[kWarps];
     uint32_t warp_eq[kWarps];
     uint32_t result[2];
-    uint32_t hist2[2048];                        // second histogram buffer (list pass 2; sampled path: pass 1)
-    uint32_t hist3[2048];                        // sampled path: radix pass 2
+    alignas(16) uint32_t hist23[4096];           // sampled path: the sample (12-bit bins), then radix
+                                                 // passes 1 and 2 in its two halves
     uint32_t bits_gt[kRegCap / 32];              // sampled path: positions with key > T
     uint32_t bits_eq[kRegCap / 32];              // sampled path: positions with key == T
 };
+
+static_assert(offsetof(TopkSmem, hist23) % 16 == 0, "the sample histogram is cleared with 16-byte stores");
 
 // Shared-memory words the sampled path needs for a row of n keys: the row,
 // rounded up to whole groups of four, then the candidate list (keys, positions).
@@ -275,10 +279,16 @@ __device__ __noinline__ void select_row_regs(TopkSmem& sm, uint32_t* stage, cons
 // Rows of up to 32768 live positions.  One thread copies the row's whole
 // groups of four into shared memory with bulk copies (the last partial group
 // by plain loads); thread t then reads groups t + 1024 j, positions
-// 4 (t + 1024 j) + c.  The first key of every group is a sample; the bin of
-// the sample histogram that holds rank r (the expected rank of the k-th
-// largest among the samples plus four standard deviations) gives a threshold
-// tau that all but rarely keeps at least k keys.  Keys >= tau are appended,
+// 4 (t + 1024 j) + c.  While the copy is in flight every thread reads up to
+// two samples, positions 16 t and 16 (t + 1024), from global memory; the
+// floor of the bin of their 12-bit histogram that holds rank r (the expected
+// rank of the k-th largest among the samples plus three standard deviations
+// and four) is a threshold tau that all but rarely keeps at least k keys.
+// (One bit finer than the radix passes' first digit: a sixteenth of the row
+// then keeps about as few extra keys as a quarter of it at 11 bits.)  Where r
+// reaches the whole sample it cannot bound the k-th key from below, and tau
+// stays 0: every key is a candidate (such rows hold under 2700 keys, within
+// the list).  Keys >= tau are appended,
 // with their positions and in no particular order, to a list after the row;
 // the exact 3-pass radix select runs on that list; the selected positions are
 // set in two bitmaps (key > T, key == T), and one block scan of the bitmap
@@ -312,23 +322,9 @@ __device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, i
     uint32_t* cand_key = buf + row_words;
     uint32_t* cand_pos = cand_key + cap;
 
-    if (tid == 0) {
+    if (tid == 0) {  // the copy goes first; this thread is the barrier's only user until the block barrier
         mbar_init(&sm.row_bar, 1);
         fence_mbar_init();
-        sm.abort = 0;
-        sm.ncand = 0;
-    }
-    if (tid < 4 && 4 * n4 + tid < row_words)  // the partial group: live scores, then zeros
-        rs[4 * n4 + tid] = 4 * n4 + tid < n ? __ldcg(row + 4 * n4 + tid) : 0.f;
-    for (int i = tid; i < 2048; i += kThreads) {  // all three histograms: no clearing barrier later
-        sm.hist[i] = 0;
-        sm.hist2[i] = 0;
-        sm.hist3[i] = 0;
-    }
-    sm.bits_gt[tid] = 0;
-    sm.bits_eq[tid] = 0;
-    __syncthreads();
-    if (tid == 0) {
         constexpr uint32_t kChunk = 32768;
         const uint32_t bytes = uint32_t(n4) * 16u;
         const uint64_t pol = l2_policy_evict_first();
@@ -336,7 +332,32 @@ __device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, i
         for (uint32_t off = 0; off < bytes; off += kChunk)
             bulk_load(reinterpret_cast<uint8_t*>(rs) + off, reinterpret_cast<const uint8_t*>(row) + off,
                       min(kChunk, bytes - off), &sm.row_bar, pol);
+        sm.abort = 0;
+        sm.ncand = 0;
+        sm.result[0] = 0;  // tau = 0 unless the sample sets it
     }
+    constexpr int kStride = 16;  // sample spacing
+    static_assert(kRegCap <= 2 * kThreads * kStride, "two samples per thread cover the longest sampled row");
+    static_assert(4 * kThreads == 4096, "each thread clears four bins of the sample histogram");
+    const int ns = (n + kStride - 1) / kStride;
+    const float s0 = tid < ns ? __ldcg(row + kStride * tid) : 0.f;
+    const float s1 = tid + kThreads < ns ? __ldcg(row + kStride * (tid + kThreads)) : 0.f;
+    if (tid < 4 && 4 * n4 + tid < row_words)  // the partial group: live scores, then zeros
+        rs[4 * n4 + tid] = 4 * n4 + tid < n ? __ldcg(row + 4 * n4 + tid) : 0.f;
+    reinterpret_cast<uint4*>(sm.hist23)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < 2048; i += kThreads) sm.hist[i] = 0;
+    sm.bits_gt[tid] = 0;
+    sm.bits_eq[tid] = 0;
+    __syncthreads();
+    const float expect = float(k) * float(ns) / float(n);
+    const int r = int(expect + 3.f * sqrtf(expect)) + 4;
+    if (r < ns) {
+        if (tid < ns) atomicAdd(&sm.hist23[order_key(s0) >> 20], 1u);
+        if (tid + kThreads < ns) atomicAdd(&sm.hist23[order_key(s1) >> 20], 1u);
+        __syncthreads();
+        select_bin_from<4096>(sm, sm.hist23, uint32_t(r));
+    }
+    const uint32_t tau = sm.result[0] << 20;
     const bool landed = mbar_wait(&sm.row_bar, 0, &sm.abort);
     if (__syncthreads_or(!landed)) {
         if (tid == 0) atomicOr(err, kErrWaitTimeout);
@@ -344,19 +365,7 @@ __device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, i
         if (!landed) mbar_wait(&sm.row_bar, 0, &sm.abort);  // once more (bounded) for the copy in flight
         return -1;
     }
-
-    // Sample histogram: the first key of every group (position 4 g < n).
     const float4* rs4 = reinterpret_cast<const float4*>(rs);
-#pragma unroll
-    for (int j = 0; j < kLoadsPerThread; ++j) {
-        const int g = tid + j * kThreads;
-        if (g < ng) atomicAdd(&sm.hist[order_key(rs4[g].x) >> 21], 1u);
-    }
-    __syncthreads();
-    const float expect = float(k) * float(ng) / float(n);
-    const int r = min(ng, int(expect + 4.f * sqrtf(expect)) + 8);
-    select_bin<2048>(sm, uint32_t(r));
-    const uint32_t tau = sm.result[0] << 21;
 
     // Candidates: bit 4 j + c of `flags` marks position 4 (tid + 1024 j) + c.  The test
     // key(v) >= tau is made in fp32 as v >= f_tau, which is the same for every non-NaN v
@@ -377,7 +386,9 @@ __device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, i
                            (live > 2 && !(v.z < f_tau) ? 4u : 0u) | (live > 3 && !(v.w < f_tau) ? 8u : 0u);
         flags |= f << (4 * j);
     }
-    clear_hist(sm);  // the sample histogram has been read (select_bin ended with a barrier)
+    // The sample histogram has been read (select_bin_from ended with a barrier): zero it for
+    // radix passes 1 and 2 (the barrier after the append orders this before them).
+    reinterpret_cast<uint4*>(sm.hist23)[tid] = make_uint4(0u, 0u, 0u, 0u);
     const uint32_t cnt = __popc(flags);
     uint32_t incl = cnt;
 #pragma unroll
@@ -402,19 +413,21 @@ __device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, i
     const int C = int(sm.ncand);
     if (C < k || C > cap) return 0;
 
-    // Exact selection on the list: pass 1 counts into hist2, pass 2 into hist3, pass 3 into hist
-    // (all three zero by now).
-    for (int i = tid; i < C; i += kThreads) atomicAdd(&sm.hist2[cand_key[i] >> 21], 1u);
+    // Exact selection on the list: passes 1 and 2 count into the halves of hist23, pass 3 into
+    // hist (all zero by now).
+    uint32_t* hist2 = sm.hist23;
+    uint32_t* hist3 = sm.hist23 + 2048;
+    for (int i = tid; i < C; i += kThreads) atomicAdd(&hist2[cand_key[i] >> 21], 1u);
     __syncthreads();
-    select_bin_from<2048>(sm, sm.hist2, uint32_t(k));
+    select_bin_from<2048>(sm, hist2, uint32_t(k));
     const uint32_t bin1 = sm.result[0];
     uint32_t kk = sm.result[1];
     for (int i = tid; i < C; i += kThreads) {
         const uint32_t ck = cand_key[i];
-        if ((ck >> 21) == bin1) atomicAdd(&sm.hist3[(ck >> 10) & 0x7FFu], 1u);
+        if ((ck >> 21) == bin1) atomicAdd(&hist3[(ck >> 10) & 0x7FFu], 1u);
     }
     __syncthreads();
-    select_bin_from<2048>(sm, sm.hist3, kk);
+    select_bin_from<2048>(sm, hist3, kk);
     const uint32_t prefix22 = (bin1 << 11) | sm.result[0];
     kk = sm.result[1];
     for (int i = tid; i < C; i += kThreads) {

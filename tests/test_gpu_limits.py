@@ -81,7 +81,7 @@ def test_past_the_limits_rejected(gpu_lib):
     assert int(buf.count_nonzero()) == 0
 
 
-@pytest.mark.parametrize("path", ["bf16", "fp8", "two_token"])
+@pytest.mark.parametrize("path", ["bf16", "fp8", "two_token", "four_token"])
 def test_short_mixed_rows_query_slots(gpu_lib, oracle, path):
     """1024 requests of one to three two-page units in a mixed order, so that consecutive rows
     start on units of either producer warp and the two query slots turn over every few units;
@@ -98,8 +98,8 @@ def test_short_mixed_rows_query_slots(gpu_lib, oracle, path):
         codes, scales = gpu_lib.to_device_fp8(f)
         ref = oracle.case_scores_fp8(f)
         run = lambda: gpu_lib.dsa_indexer_scores_fp8(q, w, codes, scales, table, seq, case.max_context, workspace=ws)
-    elif path == "two_token":
-        m = I.with_next_n(case, 2)
+    elif path in ("two_token", "four_token"):
+        m = I.with_next_n(case, 2 if path == "two_token" else 4)
         qm = torch.from_numpy(m.q.view("int16")).cuda().view(torch.bfloat16)
         wm = torch.from_numpy(m.w).cuda()
         ref = oracle.case_scores_mtp(m).reshape(-1, case.max_context // 4)

@@ -173,6 +173,26 @@ def _topk_on_rows(b, rows, n_live, k):
     return t.cpu().numpy()
 
 
+def test_topk_rows_at_the_sample_edges(gpu_lib, oracle):
+    """The sampled top-k takes its threshold from every 16th score of the row.  Rows just past
+    k (the sample cannot bound the k-th key: every key a candidate), rows of a few thousand
+    keys, and a full row whose every 16th key is 8x the others (the sampled keys are the row's
+    extremes, so too few keys pass and the exact path runs): the fused and unfused results
+    must agree with each other and with the oracle's."""
+    k = 2048
+    n_rows = [32768, k + 1, k + 13, 2600, 2900, 3100, 4500]
+    case = I.make_case(name="edges", batch=len(n_rows), max_context=131072, seq_lens=[4 * n for n in n_rows],
+                       num_pages=800, k=k, seed=31)
+    vals = I.bf16_bits_to_f32(case.key_pool)
+    t = np.arange(0, 32768, 16)
+    vals[case.page_table[0, t // 64], t % 64] *= np.float32(8.0)  # exact in bf16
+    case.key_pool = I.f32_to_bf16_bits(vals)
+    s, tk = _run_all(gpu_lib, case)
+    ref = oracle.case_scores(case)
+    check_scores(case, s, ref)
+    check_topk(case, tk, ref, gpu_scores=s)
+
+
 def test_topk_rows_that_defeat_the_sample(gpu_lib, oracle):
     """Rows where every 4th position scores high (too few keys pass the sampled threshold),
     rows with all scores equal (too many pass), heavy ties, and ragged live lengths: every
