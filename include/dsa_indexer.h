@@ -125,8 +125,11 @@ DSA_API dsa_status_t dsa_indexer_scores(const void *q, const float *w, const voi
 /*
  * Step 4 on a scores row: topk_idx [batch, k] = the min(k, n_b) positions
  * t < n_b with the largest scores[b, t] (fp32 order, -0 == +0; equal scores:
- * lower t first), in ascending t, then -1.  Reads only scores[b, t] for
- * t < n_b, and none when n_b <= k.  1 <= k <= max_context / 4.
+ * lower t first), in ascending t, then -1.  A NaN score ranks by its bits:
+ * above +inf with the sign bit clear, below -inf with it set, NaNs of one sign
+ * ordered as their bits read as an integer (larger first when positive,
+ * smaller first when negative).  Reads only scores[b, t] for t < n_b, and
+ * none when n_b <= k.  1 <= k <= max_context / 4.
  */
 DSA_API dsa_status_t dsa_indexer_topk(const float *scores, const int32_t *seq_lens, int32_t batch,
                               int64_t max_context, int32_t k, int32_t *topk_idx,

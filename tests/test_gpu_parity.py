@@ -247,6 +247,55 @@ def test_topk_infinite_scores(gpu_lib, oracle):
         np.testing.assert_array_equal(got[i], ref, err_msg=f"row {i}")
 
 
+def _topk_by_bits(row, n, k):
+    """The contract's order written out on the bits: -0 taken as +0, then a float's sign-magnitude
+    bits mapped to an unsigned key that rises with the value and extends it to NaNs (positive NaNs
+    above +inf, negative ones below -inf); the k largest keys, equal keys to the lower position,
+    listed in ascending position and padded with -1."""
+    u = row[:n].view(np.uint32).astype(np.uint64)
+    u = np.where(u == 0x80000000, 0, u)
+    key = np.where(u & 0x80000000, (~u) & 0xFFFFFFFF, u | 0x80000000)
+    order = np.lexsort((np.arange(n), -key.astype(np.int64)))[: min(k, n)]
+    out = np.full(k, -1, np.int32)
+    out[: order.size] = np.sort(order)
+    return out
+
+
+def test_topk_nan_scores(gpu_lib, oracle):
+    """NaN scores in a caller's row rank by their bits (positive NaNs above +inf, negative ones
+    below -inf, payloads in bit order), on the sampled path, its fallback and the short-row path."""
+    rng = np.random.default_rng(77)
+    M, k = 32768, 2048
+    pos_nan = (0x7FC00000 + rng.integers(0, 1 << 20, 400)).astype(np.uint32).view(np.float32)
+    neg_nan = (0xFFC00000 + rng.integers(0, 1 << 20, 400)).astype(np.uint32).view(np.float32)
+    rows, n_live = [], []
+    r = rng.standard_normal(M).astype(np.float32)
+    r[rng.choice(M, 400, replace=False)] = pos_nan          # a few hundred NaNs above everything
+    r[rng.choice(M, 50, replace=False)] = np.inf
+    rows.append(r); n_live.append(M)
+    r = rng.standard_normal(M).astype(np.float32)
+    r[rng.choice(M, 400, replace=False)] = neg_nan          # NaNs below everything: never taken
+    rows.append(r); n_live.append(M)
+    r = np.full(M, np.float32(1.0))
+    r[rng.choice(M, 3000, replace=False)] = pos_nan[rng.integers(0, 400, 3000)]  # more NaNs than k
+    rows.append(r); n_live.append(M)
+    r = rng.standard_normal(M).astype(np.float32)
+    r[0::16] = pos_nan[rng.integers(0, 400, M // 16)]       # every sampled key a NaN
+    rows.append(r); n_live.append(30001)
+    rows = np.stack(rows)
+    got = _topk_on_rows(gpu_lib, rows, n_live, k)
+    for i, n in enumerate(n_live):
+        np.testing.assert_array_equal(got[i], _topk_by_bits(rows[i], n, k), err_msg=f"row {i}")
+    # the rule agrees with the oracle on rows without NaN
+    plain = rng.standard_normal(M).astype(np.float32)
+    np.testing.assert_array_equal(_topk_by_bits(plain, M, k), oracle.topk_row(plain.astype(np.float64), M, k))
+    short = rng.standard_normal((1, 256)).astype(np.float32)
+    short[0, rng.choice(200, 30, replace=False)] = pos_nan[:30]
+    short[0, rng.choice(200, 30, replace=False)] = neg_nan[:30]
+    got = _topk_on_rows(gpu_lib, short, [200], 50)
+    np.testing.assert_array_equal(got[0], _topk_by_bits(short[0], 200, 50))
+
+
 def _signed_zero_rows(rng, M):
     """Rows whose k-th largest score is 0 and that hold both +0 and -0 (equal in fp32 order,
     so they tie and go to the lower position whatever their sign)."""
