@@ -247,6 +247,21 @@ def test_topk_infinite_scores(gpu_lib, oracle):
         np.testing.assert_array_equal(got[i], ref, err_msg=f"row {i}")
 
 
+@pytest.mark.parametrize("k", [1, 7, 100, 1000, 4096])
+def test_topk_sample_rule_across_k(gpu_lib, oracle, k):
+    """The sampled path's threshold rank depends on k and n: rows from a few hundred keys to a full
+    32768-key row, continuous and heavily tied scores, for k from 1 to 4096."""
+    rng = np.random.default_rng(500 + k)
+    M = 32768
+    n_live = [300, 1000, 2600, 5000, 20000, 32768, 32768]
+    rows = rng.standard_normal((len(n_live), M)).astype(np.float32)
+    rows[-1] = np.floor(rows[-1] * 2.0)                     # a handful of distinct values
+    got = _topk_on_rows(gpu_lib, rows, n_live, k)
+    for i, n in enumerate(n_live):
+        ref = oracle.topk_row(rows[i].astype(np.float64), n, k)
+        np.testing.assert_array_equal(got[i], ref, err_msg=f"row {i} (n = {n})")
+
+
 def _topk_by_bits(row, n, k):
     """The contract's order written out on the bits: -0 taken as +0, then a float's sign-magnitude
     bits mapped to an unsigned key that rises with the value and extends it to NaNs (positive NaNs
