@@ -288,9 +288,9 @@ __device__ __noinline__ void select_row_regs(TopkSmem& sm, uint32_t* stage, cons
 // then keeps about as few extra keys as a quarter of it at 11 bits.)  Where r
 // reaches the whole sample it cannot bound the k-th key from below, and tau
 // stays 0: every key is a candidate (such rows hold under 2700 keys, within
-// the list).  Keys >= tau are appended,
-// with their positions and in no particular order, to a list after the row;
-// the exact 3-pass radix select runs on that list; the selected positions are
+// the list).  Keys >= tau are appended, with their positions and in no
+// particular order, to a list after the row; the exact 3-pass radix select
+// runs on that list; the selected positions are
 // set in two bitmaps (key > T, key == T), and one block scan of the bitmap
 // words' bit counts gives every selected position its output slot, in
 // ascending position with the lowest positions of key T taken first.
