@@ -270,9 +270,12 @@ DSA_API dsa_status_t dsa_indexer_fused_mtp(const void *q, const float *w, const 
  *     w_w    bf16 [32, d_model]
  *     q_out  bf16 [batch, 32, 64]      (the q layout of the indexer entry points)
  *     w_out  fp32 [batch, 32]
- * Workspace: dsa_indexer_qw_proj_workspace_size(batch, d_model) bytes (header
- * plus fp32 partial sums).  The reduction over d is split across CTAs and
- * summed in a fixed order: results are deterministic.
+ * Workspace: dsa_indexer_qw_proj_workspace_size(batch, d_model) bytes (the
+ * 256-byte header with the error word; the partial sums stay on chip).  The
+ * reduction over d is split across the CTAs of a thread-block cluster and
+ * summed in a fixed order: results are deterministic.  Returns
+ * DSA_ERR_INVALID_ARG for a null or misaligned pointer or a shape outside the
+ * limits above (the workspace size query then returns 0).
  */
 #define DSA_PROJ_MAX_TOKENS 256
 

@@ -116,3 +116,105 @@ def test_topk_rejects_bad_arguments(lib, over, status):
     a.update(over)
     args = [a["scores"], a["seq"], a["batch"], a["ctx"], a["k"], a["topk"], a["ws"], a["wsb"], a["stream"]]
     assert lib.dsa_indexer_topk(*args) == status
+
+
+@pytest.mark.parametrize("over, status", [
+    (dict(batch=0), INVALID),
+    (dict(batch=1025), UNSUPPORTED),
+    (dict(codes=None), INVALID),
+    (dict(codes=A8), INVALID),                 # codes must be 16-byte aligned
+    (dict(scales=None), INVALID),
+    (dict(scales=A8), INVALID),                # scales must be 16-byte aligned
+    (dict(q=A8), INVALID),
+    (dict(pages=0), INVALID),
+    (dict(k=0), INVALID),
+    (dict(ws=None), WORKSPACE),
+])
+def test_fused_fp8_rejects_bad_arguments(lib, over, status):
+    f = lib.dsa_indexer_fused_fp8
+    f.argtypes = [P, P, P, P, ctypes.c_int64, P, P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, P, P, P,
+                  ctypes.c_size_t, P]
+    f.restype = ctypes.c_int
+    a = dict(q=A16, w=A16, codes=A16, scales=A16, pages=64, table=A16, seq=A16, batch=2, ctx=8192, k=16,
+             topk=A16, scores=None, ws=A16, wsb=1 << 30, stream=None)
+    a.update(over)
+    assert f(a["q"], a["w"], a["codes"], a["scales"], a["pages"], a["table"], a["seq"], a["batch"], a["ctx"],
+             a["k"], a["topk"], a["scores"], a["ws"], a["wsb"], a["stream"]) == status
+
+
+@pytest.mark.parametrize("over, status", [
+    (dict(next_n=0), INVALID),
+    (dict(next_n=5), INVALID),                 # 1 <= next_n <= DSA_MAX_NEXT_N = 4
+    (dict(batch=0), INVALID),
+    (dict(q=None), INVALID),
+    (dict(k=0), INVALID),
+    (dict(ws=A16 + 128), WORKSPACE),
+])
+def test_fused_mtp_rejects_bad_arguments(lib, over, status):
+    f = lib.dsa_indexer_fused_mtp
+    f.argtypes = [P, P, P, ctypes.c_int64, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, P,
+                  P, P, ctypes.c_size_t, P]
+    f.restype = ctypes.c_int
+    a = dict(q=A16, w=A16, pool=A16, pages=64, table=A16, seq=A16, batch=2, next_n=2, ctx=8192, k=16, topk=A16,
+             scores=None, ws=A16, wsb=1 << 30, stream=None)
+    a.update(over)
+    assert f(a["q"], a["w"], a["pool"], a["pages"], a["table"], a["seq"], a["batch"], a["next_n"], a["ctx"],
+             a["k"], a["topk"], a["scores"], a["ws"], a["wsb"], a["stream"]) == status
+
+
+@pytest.mark.parametrize("over, status", [
+    (dict(batch=0), INVALID),
+    (dict(batch=257), INVALID),                # past DSA_PROJ_MAX_TOKENS
+    (dict(d=32), INVALID),                     # d_model a multiple of 64
+    (dict(d=7168 + 32), INVALID),
+    (dict(x=None), INVALID),
+    (dict(x=A8), INVALID),
+    (dict(wq=A8), INVALID),
+    (dict(ww=None), INVALID),
+    (dict(qo=A4 + 1), INVALID),
+    (dict(wo=None), INVALID),
+    (dict(ws=None), WORKSPACE),
+    (dict(wsb=255), WORKSPACE),
+])
+def test_qw_proj_rejects_bad_arguments(lib, over, status):
+    f = lib.dsa_indexer_qw_proj
+    f.argtypes = [P, P, P, ctypes.c_int32, ctypes.c_int64, P, P, P, ctypes.c_size_t, P]
+    f.restype = ctypes.c_int
+    lib.dsa_indexer_qw_proj_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int64]
+    lib.dsa_indexer_qw_proj_workspace_size.restype = ctypes.c_size_t
+    a = dict(x=A16, wq=A16, ww=A16, batch=64, d=7168, qo=A16, wo=A16, ws=A16, wsb=1 << 20, stream=None)
+    a.update(over)
+    assert f(a["x"], a["wq"], a["ww"], a["batch"], a["d"], a["qo"], a["wo"], a["ws"], a["wsb"], a["stream"]) == status
+    assert lib.dsa_indexer_qw_proj_workspace_size(64, 7168) == 256
+    assert lib.dsa_indexer_qw_proj_workspace_size(0, 7168) == 0
+    assert lib.dsa_indexer_qw_proj_workspace_size(64, 100) == 0
+
+
+@pytest.mark.parametrize("over, status", [
+    (dict(batch=0), INVALID),
+    (dict(ctx=1000), INVALID),
+    (dict(q=None), INVALID),
+    (dict(q=A8), INVALID),
+    (dict(kv=A8), INVALID),
+    (dict(out=A8), INVALID),
+    (dict(lse=A4), INVALID),
+    (dict(topk=None), INVALID),
+    (dict(pages=0), INVALID),
+    (dict(k=0), INVALID),
+    (dict(k=2049), INVALID),                   # past DSA_MLA_MAX_TOPK
+    (dict(scale=float("nan")), INVALID),
+    (dict(scale=float("inf")), INVALID),
+    (dict(ws=None), WORKSPACE),
+    (dict(wsb=0), WORKSPACE),
+    (dict(pages=1 << 25), UNSUPPORTED),        # cache rows past 32-bit coordinates
+])
+def test_sparse_mla_rejects_bad_arguments(lib, over, status):
+    f = lib.dsa_sparse_mla_decode
+    f.argtypes = [P, P, ctypes.c_int64, P, P, ctypes.c_int32, ctypes.c_int64, P, ctypes.c_int32, ctypes.c_float,
+                  P, P, P, ctypes.c_size_t, P]
+    f.restype = ctypes.c_int
+    a = dict(q=A16, kv=A16, pages=64, table=A16, seq=A16, batch=2, ctx=8192, topk=A16, k=64, scale=0.04,
+             out=A16, lse=A16, ws=A16, wsb=1 << 30, stream=None)
+    a.update(over)
+    assert f(a["q"], a["kv"], a["pages"], a["table"], a["seq"], a["batch"], a["ctx"], a["topk"], a["k"], a["scale"],
+             a["out"], a["lse"], a["ws"], a["wsb"], a["stream"]) == status
