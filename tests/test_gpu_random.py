@@ -1,7 +1,7 @@
 """GPU parity on seeded random shapes: batch, max_context, lengths (including 0, 1..3 tokens, a
 full row and a partial last page) and k drawn at random, through the scores, top-k and both
-fused entry points (which must agree bit for bit), and through the multi-token entry points;
-every result against the fp64 oracle."""
+fused entry points (which must agree bit for bit), the multi-token and fp8 entry points, and the
+sparse-MLA decode over random top-k rows; every result against the fp64 oracle."""
 import numpy as np
 import pytest
 
@@ -52,3 +52,29 @@ def test_random_shapes_multi_token(gpu_lib, oracle, seed):
     f = _flat(case)
     check_scores(f, s.reshape(B * Q, -1), ref.reshape(B * Q, -1))
     check_topk(f, t.reshape(B * Q, -1), ref.reshape(B * Q, -1), gpu_scores=s.reshape(B * Q, -1))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_shapes_fp8(gpu_lib, oracle, seed):
+    from test_gpu_fp8 import _run_fp8
+    case = I.with_fp8_keys(_random_case(200 + seed))
+    s, t, err = _run_fp8(gpu_lib, case)
+    assert err == 0
+    ref = oracle.case_scores_fp8(case)
+    check_scores(case, s, ref)
+    check_topk(case, t, ref, gpu_scores=s)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_shapes_sparse_mla(gpu_lib, oracle, seed):
+    """The decode over random top-k rows (holes, positions past the live length, duplicates) of a
+    random indexer case: k from 1 to 2048, batches that take one or several splits per request."""
+    from test_gpu_mla import _check, _run
+    case = _random_case(300 + seed)
+    rng = np.random.default_rng(9000 + seed)
+    k = int(rng.integers(1, 2049))
+    M = case.max_context // 4
+    topk = rng.integers(-1, M, size=(case.batch, k)).astype(np.int32)  # -1 holes, any position
+    mc = I.mla_case(case, topk)
+    o, lse = _run(gpu_lib, mc)
+    _check(o, lse, mc, oracle)
