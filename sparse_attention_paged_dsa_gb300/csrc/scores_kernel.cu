@@ -69,16 +69,17 @@ using namespace scores;
 // TMA-issuing producer warps each: one issuing thread keeps too few page
 // boxes in flight to cover HBM latency (a TMA instruction takes about 120
 // cycles to issue), so each SM runs six issuers, with three stages each (four
-// measured the same: at this depth the ring is not the limit).  Q >= 2: the
-// Q x 4 KiB query tiles and the 32 Q-column accumulators need two CTAs per SM
-// (four stages).
+// measured the same: at this depth the ring is not the limit).  Q = 2: also
+// three CTAs per SM (three stages, two 64-column accumulators each, so that
+// three CTAs' TMEM fits).  Q >= 3: the 32 Q-column accumulators need the TMEM
+// of two CTAs per SM (four stages).
 template <int Q, int S>
 struct Cfg {
-    static constexpr int kCtasPerSm = Q == 1 ? 3 : 2;
+    static constexpr int kCtasPerSm = Q <= 2 ? 3 : 2;  // Q >= 3: the accumulators need the TMEM of 2
     static constexpr int kStages = S;                         // 16 KiB stages per CTA, shared by the producers
     static constexpr int kEpiGroups = Q >= 3 ? 2 : 1;         // epilogue groups of 4 warps (Q >= 3: Q passes per unit)
     static constexpr int kQSlots = 2;
-    static constexpr int kAccStages = Q <= 2 ? 4 : 2;
+    static constexpr int kAccStages = Q == 1 ? 4 : 2;
     static constexpr int kMetaRing = 16;                      // >= kStages + kAccStages + 1
     static constexpr int kAccCols = 32 * Q;                   // fp32 columns per accumulator (N = 32 Q heads)
     static constexpr uint32_t kTmemCols =                     // power of two >= 32
@@ -121,7 +122,7 @@ struct Layout {
     // Whether kCtasPerSm CTAs fit one SM's shared memory for this batch.
     static constexpr bool fits(int batch) { return bytes(batch) * Cfg<Q, S>::kCtasPerSm <= 226 * 1024; }
 };
-static_assert(Layout<1, 3>::fits(kMaxBatch) && Layout<2, 4>::fits(kMaxBatch) && Layout<3, 4>::fits(kMaxBatch) &&
+static_assert(Layout<1, 3>::fits(kMaxBatch) && Layout<2, 3>::fits(kMaxBatch) && Layout<3, 4>::fits(kMaxBatch) &&
                   Layout<4, 4>::fits(kMaxBatch),
               "shared memory budget per SM");
 
@@ -524,7 +525,7 @@ cudaError_t launch_scores(const CUtensorMap& keys_map, const CUtensorMap& q_map,
                           cudaStream_t stream) {
     switch (p.tokens) {
         case 1: return launch_scores_q<1, 3>(keys_map, q_map, p, stream);
-        case 2: return launch_scores_q<2, 4>(keys_map, q_map, p, stream);
+        case 2: return launch_scores_q<2, 3>(keys_map, q_map, p, stream);
         case 3: return launch_scores_q<3, 4>(keys_map, q_map, p, stream);
         case 4: return launch_scores_q<4, 4>(keys_map, q_map, p, stream);
     }
