@@ -13,8 +13,8 @@
 // positions); every key > T and those keys == T are written in ascending
 // position.  One 1024-thread CTA per request.
 //   * n_b <= 32768, first choice (sampled path): the row is copied into shared
-//     memory by the bulk-copy engine; meanwhile a histogram of every 16th key,
-//     read straight from global memory, gives a threshold that keeps a little
+//     memory by the bulk-copy engine; meanwhile a histogram of a sixteenth of
+//     the keys (four in every 64), read straight from global memory, gives a threshold that keeps a little
 //     more than k keys; once the row has landed those are appended with
 //     their positions to a short list, the radix passes run on that list
 //     only, and the selected positions are marked in bitmaps whose prefix
@@ -279,9 +279,9 @@ __device__ __noinline__ void select_row_regs(TopkSmem& sm, uint32_t* stage, cons
 // Rows of up to 32768 live positions.  One thread copies the row's whole
 // groups of four into shared memory with bulk copies (the last partial group
 // by plain loads); thread t then reads groups t + 1024 j, positions
-// 4 (t + 1024 j) + c.  While the copy is in flight every thread reads up to
-// two samples, positions 16 t and 16 (t + 1024), from global memory; the
-// floor of the bin of their 12-bit histogram that holds rank r (the expected
+// 4 (t + 1024 j) + c.  While the copy is in flight thread t reads the four
+// samples at positions 64 t .. 64 t + 3 from global memory; the floor of the
+// bin of their 12-bit histogram that holds rank r (the expected
 // rank of the k-th largest among the samples plus three standard deviations
 // and four) is a threshold tau that all but rarely keeps at least k keys.
 // (One bit finer than the radix passes' first digit: a sixteenth of the row
@@ -300,6 +300,10 @@ __device__ __noinline__ void select_row_regs(TopkSmem& sm, uint32_t* stage, cons
 // limit (error bit set, the row padded with -1).
 // (With an L2 eviction policy: the scores kernels store the row evict-last so that it waits in L2
 // for this read; reading it evict-first hands those lines back.)
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar,
                                           uint64_t policy) {
     asm volatile(
@@ -336,12 +340,18 @@ __device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, i
         sm.ncand = 0;
         sm.result[0] = 0;  // tau = 0 unless the sample sets it
     }
-    constexpr int kStride = 16;  // sample spacing
-    static_assert(kRegCap <= 2 * kThreads * kStride, "two samples per thread cover the longest sampled row");
+    // Samples: the four scores at positions 64 g .. 64 g + 3 of every group g (thread g), one
+    // 16-byte load each, so that the sample takes a quarter of the load slots that one score in
+    // sixteen read one by one would, beside the copy.  In bounds: 64 g < n and the row width
+    // is a multiple of 64.
+    constexpr int kGroupStride = 64;
+    static_assert(kRegCap <= kGroupStride * kThreads, "one sample group per thread covers the longest sampled row");
     static_assert(4 * kThreads == 4096, "each thread clears four bins of the sample histogram");
-    const int ns = (n + kStride - 1) / kStride;
-    const float s0 = tid < ns ? __ldcg(row + kStride * tid) : 0.f;
-    const float s1 = tid + kThreads < ns ? __ldcg(row + kStride * (tid + kThreads)) : 0.f;
+    const int n_groups = (n + kGroupStride - 1) / kGroupStride;
+    const int ns = (n / kGroupStride) * 4 + min(n % kGroupStride, 4);  // live samples
+    const int mine = tid < n_groups ? min(n - kGroupStride * tid, 4) : 0;
+    const float4 sv = tid < n_groups ? __ldcg(reinterpret_cast<const float4*>(row + kGroupStride * tid))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid < 4 && 4 * n4 + tid < row_words)  // the partial group: live scores, then zeros
         rs[4 * n4 + tid] = 4 * n4 + tid < n ? __ldcg(row + 4 * n4 + tid) : 0.f;
     reinterpret_cast<uint4*>(sm.hist23)[tid] = make_uint4(0u, 0u, 0u, 0u);
@@ -352,8 +362,10 @@ __device__ __forceinline__ int select_row_sampled(TopkSmem& sm, uint32_t* buf, i
     const float expect = float(k) * float(ns) / float(n);
     const int r = int(expect + 3.f * sqrtf(expect)) + 4;
     if (r < ns) {
-        if (tid < ns) atomicAdd(&sm.hist23[order_key(s0) >> 20], 1u);
-        if (tid + kThreads < ns) atomicAdd(&sm.hist23[order_key(s1) >> 20], 1u);
+        if (mine > 0) atomicAdd(&sm.hist23[order_key(sv.x) >> 20], 1u);
+        if (mine > 1) atomicAdd(&sm.hist23[order_key(sv.y) >> 20], 1u);
+        if (mine > 2) atomicAdd(&sm.hist23[order_key(sv.z) >> 20], 1u);
+        if (mine > 3) atomicAdd(&sm.hist23[order_key(sv.w) >> 20], 1u);
         __syncthreads();
         select_bin_from<4096>(sm, sm.hist23, uint32_t(r));
     }
@@ -587,7 +599,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
     extern __shared__ __align__(16) uint32_t cache[];
     __shared__ TopkSmem sm;
     // Launched as a programmatic dependent of the scores kernel: wait for its
-    // results before touching global memory.
+    // results before reading global memory.  Before the wait, L2 prefetches of
+    // the row, its length and its output (no data is consumed, and L2 is where
+    // the scores kernel's writes land) let the SM translate those addresses
+    // while the scores kernel finishes.
+    if (threadIdx.x == 0) prefetch_l2(p.seq_lens + blockIdx.x / p.tokens);
+    if (threadIdx.x == 32) prefetch_l2(p.scores + int64_t(blockIdx.x) * p.row_width);
+    if (threadIdx.x == 64) prefetch_l2(p.out + int64_t(blockIdx.x) * p.k);
     pdl_wait_prior_grid();
     pdl_allow_next_grid();
     const int b = blockIdx.x;  // row: request b / tokens, query token b % tokens

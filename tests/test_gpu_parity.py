@@ -174,9 +174,10 @@ def _topk_on_rows(b, rows, n_live, k):
 
 
 def test_topk_rows_at_the_sample_edges(gpu_lib, oracle):
-    """The sampled top-k takes its threshold from every 16th score of the row.  Rows just past
-    k (the sample cannot bound the k-th key: every key a candidate), rows of a few thousand
-    keys, and a full row whose every 16th key is 8x the others (the sampled keys are the row's
+    """The sampled top-k takes its threshold from a sixteenth of the row's scores, the four at
+    positions 64 g .. 64 g + 3 of every group g.  Rows just past k (the sample cannot bound the
+    k-th key: every key a candidate), rows of a few thousand keys, and a full row whose sampled
+    keys are 8x the others (the sampled keys are the row's
     extremes, so too few keys pass and the exact path runs): the fused and unfused results
     must agree with each other and with the oracle's."""
     k = 2048
@@ -184,7 +185,8 @@ def test_topk_rows_at_the_sample_edges(gpu_lib, oracle):
     case = I.make_case(name="edges", batch=len(n_rows), max_context=131072, seq_lens=[4 * n for n in n_rows],
                        num_pages=800, k=k, seed=31)
     vals = I.bf16_bits_to_f32(case.key_pool)
-    t = np.arange(0, 32768, 16)
+    t = np.arange(0, 32768)
+    t = t[t % 64 < 4]                                              # the sampled positions
     vals[case.page_table[0, t // 64], t % 64] *= np.float32(8.0)  # exact in bf16
     case.key_pool = I.f32_to_bf16_bits(vals)
     s, tk = _run_all(gpu_lib, case)
@@ -194,14 +196,17 @@ def test_topk_rows_at_the_sample_edges(gpu_lib, oracle):
 
 
 def test_topk_rows_that_defeat_the_sample(gpu_lib, oracle):
-    """Rows where every 4th position scores high (too few keys pass the sampled threshold),
-    rows with all scores equal (too many pass), heavy ties, and ragged live lengths: every
+    """Rows where the sampled positions score high (too few keys pass the sampled threshold),
+    where every 4th position does, rows with all scores equal (too many pass), heavy ties, and ragged live lengths: every
     path of the top-k kernel must give the exact top-k (ties to the lower position)."""
     rng = np.random.default_rng(99)
     M, k = 32768, 2048
     rows, n_live = [], []
     r = rng.standard_normal(M).astype(np.float32)
     r[0::4] += 100.0
+    rows.append(r); n_live.append(M)                       # a quarter of the row (and of the sample) high
+    r = rng.standard_normal(M).astype(np.float32)
+    r[np.arange(M) % 64 < 4] += 100.0
     rows.append(r); n_live.append(M)                       # samples all high: fallback (too few)
     rows.append(np.full(M, 1.5, np.float32)); n_live.append(M)   # one value: fallback (too many)
     rows.append(np.floor(rng.standard_normal(M) * 3).astype(np.float32)); n_live.append(M)  # ties
@@ -295,7 +300,7 @@ def test_topk_nan_scores(gpu_lib, oracle):
     r[rng.choice(M, 3000, replace=False)] = pos_nan[rng.integers(0, 400, 3000)]  # more NaNs than k
     rows.append(r); n_live.append(M)
     r = rng.standard_normal(M).astype(np.float32)
-    r[0::16] = pos_nan[rng.integers(0, 400, M // 16)]       # every sampled key a NaN
+    r[np.arange(M) % 64 < 4] = pos_nan[rng.integers(0, 400, M // 16)]  # every sampled key a NaN
     rows.append(r); n_live.append(30001)
     rows = np.stack(rows)
     got = _topk_on_rows(gpu_lib, rows, n_live, k)
