@@ -38,16 +38,19 @@
 //     stage's full barrier (a TMA instruction costs about as much issue time
 //     as a whole page, so the small scale rows do not go through TMA).  Per
 //     request change the owner of the first unit stages the bf16 query and
-//     its head weights (TMA) for the splitter.
-//   * warp 2: per request change, splits the query into the hi and lo e4m3
-//     tiles the MMA reads (64-byte swizzle) and w_h * S_h, in a small ring
-//     that the epilogue frees when it leaves the request.
+//     its head weights (TMA) for the splitters.
+//   * warps 8 and 9: per request change, split the query into the hi and lo
+//     e4m3 tiles the MMA reads (64-byte swizzle) and w_h * S_h, in a small
+//     ring that the epilogue frees when it leaves the request.  The split is
+//     on the path to each request's first MMA, so two warps share it, each
+//     thread taking half of one head.
+//   * warp 2: the -inf fill of the rows' dead parts (full-width rows), with
+//     the same flat per-CTA share as the bf16 kernel's set-up warp.
 //   * warp 1: tcgen05.mma kind::f8f6f4, M=128 keys x N=32 heads x K=32, four
 //     per unit (hi then lo, two K-slices each), into one of 4 TMEM
 //     accumulators of 32 columns.
 //   * warps 4-7: tcgen05.ld, relu, weighted head sum, key scale, live mask,
-//     128-byte stores.  The -inf fill of the rows' dead parts (full-width
-//     rows) is the splitter's, after its first split.
+//     128-byte stores.
 //   * Every wait is bounded (about 1 s); a timeout sets an error bit, stops
 //     all roles, drains in-flight copies and MMAs and frees TMEM.
 #include <cuda.h>
@@ -78,9 +81,10 @@ constexpr int kRing = 16;        // metadata and scale ring, >= S + kAccStages +
 constexpr int kCtasPerSm = 3;
 constexpr int kAccCols = 32;     // N = 32 heads
 constexpr uint32_t kTmemCols = kAccStages * kAccCols;  // 128
-constexpr int kConvThreads = 32;
+constexpr int kSplitWarps = 2;                  // warps 8, 9
+constexpr int kConvThreads = 32 * kSplitWarps;
 constexpr int kEpiThreads = 128;
-constexpr int kThreads = 128 + kEpiThreads;                // producers 0 and 3, MMA 1, splitter 2, epilogue 4..7
+constexpr int kThreads = 128 + kEpiThreads + kConvThreads;  // producers 0 and 3, MMA 1, fill 2, epilogue 4..7, splitters 8, 9
 constexpr int kStageBytes = 2 * kPageCodeBytes;            // 8 KiB: 128 keys x 64 B
 constexpr int kQHalfBytes = kHeads * kHeadDim;             // 2 KiB: 32 heads x 64 B (hi or lo)
 constexpr int kQ8Bytes = 2 * kQHalfBytes;                  // hi tile, then lo tile
@@ -106,6 +110,8 @@ struct __align__(16) SmemCtl {
     int abort;
     int32_t meta[kRing];
     int32_t qrow[kQRaw];                      // request of each staged query (-1: no more)
+    int32_t split_flag[kSplitWarps];          // each splitter warp's view of the current raw query
+    __align__(8) uint32_t split_amax[kHeads][kSplitWarps];  // partial max |q| bits per head and warp
     __align__(16) float wq[kQSlots][kHeads];  // w_h * S_h of each split query
 };
 
@@ -136,6 +142,9 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+
+// Named barrier 1 over the splitter warps.
+__device__ __forceinline__ void split_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConvThreads) : "memory"); }
 
 // Two floats to two e4m3 codes (round to nearest even, saturating); `lo_val` in the low byte.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo_val, float hi_val) {
@@ -232,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // lane 0 posts the metadata and issues the two code boxes; all 32 lanes copy the
         // unit's scales (cp.async, arriving on the stage's full barrier).  A row change is
         // numbered in sequence order; warp 0 stages every row's query and head weights for the
-        // splitter, in that order, so that its waits on a raw-query slot are one phase apart.
+        // splitters, in that order, so that its waits on a raw-query slot are one phase apart.
         const int me = warp == 0 ? 0 : 1;
         const uint64_t pol_keys = l2_policy_evict_first();
         const uint64_t pol_q = l2_policy_evict_last();
@@ -258,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     prev_b = bi;
                 }
                 int failed = 0;
-                if (new_row && me == 0) {  // stage the request's query and head weights for the splitter
+                if (new_row && me == 0) {  // stage the request's query and head weights for the splitters
                     if (lane == 0) {
                         const int k = nrows - 1, qs = k % kQRaw;
                         if (!mbar_wait(&ctl.qraw_empty[qs], ((k / kQRaw) & 1) ^ 1u, &ctl.abort)) {
@@ -322,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             cur_cnt = nxt_cnt;
             cur = nxt;
         }
-        // End-of-work markers: the splitter's (row-change number nrows) from warp 0, which
+        // End-of-work markers: the splitters' (row-change number nrows) from warp 0, which
         // stages every query; the MMA issuer's and epilogue's (unit number seq) from the warp
         // that owns that place.
         if (!stop && me == 0) {
@@ -425,32 +434,60 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         __syncwarp();
     } else if (warp == 2) {
-        // ================= query splitter: bf16 q -> hi/lo e4m3 tile and w_h * S_h =================
-        // After the first split (the first MMA waits for it) this warp also streams the CTA's
-        // share of the -inf fill of the rows' dead parts when a full-width row is requested.
-        const int h = lane;  // head
-        bool stop = false, filled = !p.fill_dead;
+        // ================= the -inf fill of the rows' dead parts (full-width rows) =================
+        if (p.fill_dead) fill_dead_tails_warp(rows, p, lane);
+    } else if (warp >= 8) {
+        // ================= query splitters: bf16 q -> hi/lo e4m3 tile and w_h * S_h =================
+        // Two warps split each request's query: thread (sw, h) takes two of head h's four
+        // 16-element chunks, c and c ^ 2 with c = (sw + h) mod 2 + 2 ((h >> 1) mod 2), and loads
+        // the first or second 16-byte half of a chunk first by (h >> 2) mod 2, so that every
+        // shared-memory access of a warp spreads over all eight 16-byte bank groups (one lane
+        // per head reading whole rows hit one group 32 times).  The two partial maxima of a head
+        // meet in shared memory.  Every splitter thread reaches both named barriers of every
+        // round, so a wait that fails in one warp stops both together.
+        const int sw = warp - 8;
+        const int h = lane;
+        const int c = ((sw + h) & 1) + 2 * ((h >> 1) & 1);
+        const int v0 = (h >> 2) & 1;  // the chunk half loaded first
+        bool stop = false;
         for (int j = 0;; ++j) {
-            const int rs = j % kQRaw;
-            if (!mbar_wait(&ctl.qraw_full[rs], (j / kQRaw) & 1, &ctl.abort)) {
+            const int rs = j % kQRaw, qs = j % kQSlots;
+            bool ok = mbar_wait(&ctl.qraw_full[rs], (j / kQRaw) & 1, &ctl.abort);
+            const bool end = ok && ctl.qrow[rs] < 0;
+            if (ok && !end) ok = mbar_wait(&ctl.q8_empty[qs], ((j / kQSlots) & 1) ^ 1u, &ctl.abort);
+            if (lane == 0) ctl.split_flag[sw] = ok ? (end ? 2 : 1) : 0;
+            split_bar_sync();
+            const int fmin = min(ctl.split_flag[0], ctl.split_flag[1]);
+            if (fmin == 0) {
                 stop = true;
                 break;
             }
-            if (ctl.qrow[rs] < 0) break;
-            const int qs = j % kQSlots;
-            if (!mbar_wait(&ctl.q8_empty[qs], ((j / kQSlots) & 1) ^ 1u, &ctl.abort)) {
-                stop = true;
-                break;
+            if (fmin == 2) break;  // the end marker
+            // Thread (sw, h): chunks c and c ^ 2 of head h, c = (sw + h) mod 2 + 2 ((h >> 1) mod 2).
+            const uint8_t* hrow = qraw + size_t(rs) * kQRowBytes + h * 128;
+            uint4 u[2][2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint4* src = reinterpret_cast<const uint4*>(hrow + (c ^ (2 * k)) * 32);
+                const uint4 ua = src[v0], ub = src[v0 ^ 1];
+                u[k][0] = v0 ? ub : ua;
+                u[k][1] = v0 ? ua : ub;
             }
-            const uint4* src = reinterpret_cast<const uint4*>(qraw + size_t(rs) * kQRowBytes + h * 128);
-            uint32_t amax_bits = 0;  // max |q| over the head, on the bf16 magnitude bits
+            uint32_t amax_bits = 0;  // max |q| over the two chunks, on the bf16 magnitude bits
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                const uint4 u = src[v];
-                const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
+            for (int k = 0; k < 2; ++k)
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    amax_bits = max(amax_bits, max(wds[i] & 0x7FFFu, (wds[i] >> 16) & 0x7FFFu));
+                for (int v = 0; v < 2; ++v) {
+                    const uint32_t wds[4] = {u[k][v].x, u[k][v].y, u[k][v].z, u[k][v].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        amax_bits = max(amax_bits, max(wds[i] & 0x7FFFu, (wds[i] >> 16) & 0x7FFFu));
+                }
+            ctl.split_amax[h][sw] = amax_bits;
+            split_bar_sync();
+            {
+                const uint2 m2 = *reinterpret_cast<const uint2*>(ctl.split_amax[h]);
+                amax_bits = max(m2.x, m2.y);
             }
             // S_h = 2^(e - 7) with e the exponent of the head's largest magnitude (clamped so
             // that S_h and 1 / S_h are normal floats); all-zero heads take e = 0.
@@ -460,40 +497,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const float s_h = __uint_as_float(uint32_t(127 + e - 7) << 23);
             uint8_t* tile = q8 + size_t(qs) * kQ8Bytes;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {  // 16-byte chunk c of rows 2h (hi) and 2h + 1 (lo)
+            for (int k = 0; k < 2; ++k) {
+                const int ck = c ^ (2 * k);
                 float x[16];
+                const uint32_t wds[8] = {u[k][0].x, u[k][0].y, u[k][0].z, u[k][0].w,
+                                         u[k][1].x, u[k][1].y, u[k][1].z, u[k][1].w};
 #pragma unroll
-                for (int v = 0; v < 2; ++v) {
-                    const uint4 u = src[2 * c + v];
-                    const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        x[8 * v + 2 * i] = __uint_as_float(wds[i] << 16) * inv_s;
-                        x[8 * v + 2 * i + 1] = __uint_as_float(wds[i] & 0xFFFF0000u) * inv_s;
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    x[2 * i] = __uint_as_float(wds[i] << 16) * inv_s;
+                    x[2 * i + 1] = __uint_as_float(wds[i] & 0xFFFF0000u) * inv_s;
                 }
                 uint2 hi0, lo0, hi1, lo1;
                 split8(x, hi0, lo0);
                 split8(x + 8, hi1, lo1);
-                const int sw = (c ^ ((h >> 1) & 3)) << 4;  // 64-byte swizzle: 16-byte chunk c of row h
-                *reinterpret_cast<uint4*>(tile + h * 64 + sw) = make_uint4(hi0.x, hi0.y, hi1.x, hi1.y);
-                *reinterpret_cast<uint4*>(tile + kQHalfBytes + h * 64 + sw) = make_uint4(lo0.x, lo0.y, lo1.x, lo1.y);
+                const int swz = (ck ^ ((h >> 1) & 3)) << 4;  // 64-byte swizzle: 16-byte chunk ck of row h
+                *reinterpret_cast<uint4*>(tile + h * 64 + swz) = make_uint4(hi0.x, hi0.y, hi1.x, hi1.y);
+                *reinterpret_cast<uint4*>(tile + kQHalfBytes + h * 64 + swz) = make_uint4(lo0.x, lo0.y, lo1.x, lo1.y);
             }
-            ctl.wq[qs][h] = wraw[rs * kHeads + h] * s_h;
+            if (sw == 0) ctl.wq[qs][h] = wraw[rs * kHeads + h] * s_h;
             mbar_arrive(&ctl.qraw_empty[rs]);
             fence_proxy_async_smem();
             mbar_arrive(&ctl.q8_full[qs]);
-            if (!filled) {
-                fill_dead_tails_warp(rows, p, lane);
-                filled = true;
-            }
         }
-        if (!filled && !stop) fill_dead_tails_warp(rows, p, lane);  // a CTA without units
         if (stop && lane == 0) {
             atomicOr(p.err, kErrWaitTimeout);
             ctl.abort = 1;
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 8) {
         // ================= epilogue: warps 4..7 =================
         const int quad = warp & 3;         // TMEM lanes [32*quad, 32*quad + 32)
         const float neg_inf = __int_as_float(0xff800000);
