@@ -231,3 +231,27 @@ def test_fp8_query_dynamic_range(gpu_lib, oracle):
     n5 = int(case.live_positions()[5])
     assert np.all(np.isfinite(s[5, :n5])) and np.all(np.isneginf(s[5, n5:]))
     np.testing.assert_allclose(s[5, :n5], ref[5, :n5], rtol=0, atol=float(np.abs(ref[5, :n5]).max()) * 3e-3 + 1e-44)
+
+
+def test_fp8_many_short_requests(gpu_lib, oracle):
+    """Every CTA of the persistent grid starts several requests (1024 requests of one to three
+    units each), so the query-split ring turns over at nearly every unit; each request's query
+    sits at its own power-of-two magnitude (2^-40 .. 2^40) with some heads all zero, so a split
+    that used another request's scale or tile would miss the tolerance by orders of magnitude."""
+    rng = np.random.default_rng(21)
+    B = 1024
+    seq = rng.integers(1, 1537, size=B)                      # up to 384 C4 positions: 1 to 3 units
+    seq[::97] = 0                                            # a few empty requests
+    base = I.with_fp8_keys(I.make_case(name="short_many", batch=B, max_context=2048, seq_lens=seq,
+                                       num_pages=B * 8 + 16, k=16, seed=23))
+    q = I.bf16_bits_to_f32(base.q).astype(np.float64)
+    q *= (2.0 ** rng.integers(-40, 41, size=B))[:, None, None]
+    q[rng.random(B) < 0.2, ::3] = 0.0                        # some requests with every third head zero
+    case = I.IndexerCase("short_many", I.f32_to_bf16_bits(q.astype(np.float32)), base.w, base.key_pool,
+                         base.page_table, base.seq_lens, base.max_context, base.k,
+                         key_codes=base.key_codes, key_scales=base.key_scales)
+    s, t, err = _run_fp8(gpu_lib, case)
+    assert err == 0
+    ref = oracle.case_scores_fp8(case)
+    check_scores(case, s, ref)
+    check_topk(case, t, ref, gpu_scores=s)

@@ -369,3 +369,23 @@ def test_topk_signed_zeros_tie(gpu_lib, oracle):
     for i in range(rows.shape[0]):
         ref = oracle.topk_row(pad[i].astype(np.float64), M, k)
         np.testing.assert_array_equal(t[i], ref, err_msg=f"multi-token row {i}")
+
+
+def test_many_short_requests(gpu_lib, oracle):
+    """1024 requests of one to three units each: every CTA of the persistent grid starts several
+    requests, so the query-tile ring and the epilogue's head weights turn over at nearly every
+    unit; each request's query sits at its own power-of-two magnitude (2^-40 .. 2^40), so a unit
+    scored with another request's query or weights would miss the tolerance by orders of magnitude."""
+    rng = np.random.default_rng(22)
+    B = 1024
+    seq = rng.integers(1, 1537, size=B)
+    seq[::89] = 0
+    base = I.make_case(name="short_many_bf16", batch=B, max_context=2048, seq_lens=seq, num_pages=B * 8 + 16,
+                       k=16, seed=24)
+    q = I.bf16_bits_to_f32(base.q).astype(np.float64) * (2.0 ** rng.integers(-40, 41, size=B))[:, None, None]
+    case = I.IndexerCase("short_many_bf16", I.f32_to_bf16_bits(q.astype(np.float32)), base.w, base.key_pool,
+                         base.page_table, base.seq_lens, base.max_context, base.k)
+    s, t = _run_all(gpu_lib, case)
+    ref = oracle.case_scores(case)
+    check_scores(case, s, ref)
+    check_topk(case, t, ref, gpu_scores=s)
