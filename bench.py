@@ -250,13 +250,25 @@ def evict_l2(buf):
     torch.amax(buf)
 
 
+def device_preroll(stream):
+    """Keep the device busy for about 100 us on `stream` (a spin kernel), so that the host has
+    submitted the start event and the graph behind it before the device reaches them: the event
+    pair then brackets the device's execution of the steps, not the host's graph submission."""
+    import torch
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        with torch.cuda.stream(stream):
+            sleep(200_000)
+
+
 def time_loop(fn, n, stream, flush=None):
     """CUDA-event time of `n` back-to-back calls of `fn` on `stream`.
 
     Without `flush`: the `n` calls are captured in one CUDA graph (a serving loop's
     form: no host launch cost between calls, consecutive launches overlap through
     programmatic dependent launch), replayed once untimed, then once between one
-    event pair; returns (mean seconds per call, None).  With `flush` (a callable
+    event pair, behind a device pre-roll that keeps the host's graph submission out of
+    the region; returns (mean seconds per call, None).  With `flush` (a callable
     that evicts L2): events around every call, the flush outside them; returns
     (mean, per-call list)."""
     import torch
@@ -275,6 +287,7 @@ def time_loop(fn, n, stream, flush=None):
             g.replay()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        device_preroll(stream)
         e0.record(stream)
         with torch.cuda.stream(stream):
             g.replay()
@@ -322,6 +335,7 @@ def graph_us_per_call(fn, reps=20, replays=20):
     times = []
     for _ in range(replays):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        device_preroll(torch.cuda.current_stream())
         e0.record()
         g.replay()
         e1.record()
@@ -797,7 +811,7 @@ def run_ours(args):
                                                            " (separate loop, an event between steps)")},
         "step_gbs_live_keys": live * KEY_BYTES_PER_POSITION / mean_step / 1e9,
         "timing": ("events around every step, L2 flushed outside them" if args.l2_flush else
-                   "the K back-to-back steps captured in one CUDA graph, one replay between one CUDA-event pair"),
+                   "the K back-to-back steps captured in one CUDA graph, one replay between one CUDA-event pair (a ~100 us device spin before the start event keeps the host's graph submission out of the region)"),
         "cpu_baseline": cpu,
         "context_scaling": scaling_1m,
         "configs": configs,
