@@ -20,10 +20,14 @@
 // quantum 2^-9.  So every element within a factor 2^9 of its head's largest
 // one is represented exactly, and smaller ones keep an absolute error of at
 // most 2^-10 in units of S_h, below 2^-17 of the head's largest element.
-// The two terms are two K-halves of one contraction: four MMAs of K = 32
-// accumulate  acc[h] = sum_d code_t,d * (hi_h,d + lo_h,d)  into one fp32
-// column per head (N = 32), so
+// The hi rows and the lo rows of the split query are stacked into one
+// N = 64 operand (hi heads 0..31, then lo heads 0..31), so two MMAs of K = 32
+// per unit accumulate  hi_acc[h] = sum_d code_t,d * hi_h,d  and lo_acc[h]
+// into two fp32 columns per head, and with acc[h] = hi_acc[h] + lo_acc[h]
 //     q_h . k_t = S_h * scale_t * acc[h].
+// (Each tcgen05.mma costs about as much of a unit's time as its data: four
+// MMAs of N = 32 per unit, hi and lo in turn into one column, ran 1 us
+// slower on the dense 128K workload.)
 // S_h and scale_t are positive, so relu commutes with them: the epilogue
 // forms w_h * S_h * relu(acc[h]), sums over heads and multiplies by scale_t
 // once.
@@ -46,9 +50,9 @@
 //     thread taking half of one head.
 //   * warp 2: the -inf fill of the rows' dead parts (full-width rows), with
 //     the same flat per-CTA share as the bf16 kernel's set-up warp.
-//   * warp 1: tcgen05.mma kind::f8f6f4, M=128 keys x N=32 heads x K=32, four
-//     per unit (hi then lo, two K-slices each), into one of 4 TMEM
-//     accumulators of 32 columns.
+//   * warp 1: tcgen05.mma kind::f8f6f4, M=128 keys x N=64 (hi, lo) x K=32,
+//     two per unit (the two K-slices), into one of 2 TMEM accumulators of 64
+//     columns (three CTAs' accumulators fill 384 of the SM's 512 columns).
 //   * warps 4-7: tcgen05.ld, relu, weighted head sum, key scale, live mask,
 //     128-byte stores.
 //   * Every wait is bounded (about 1 s); a timeout sets an error bit, stops
@@ -76,10 +80,10 @@ using namespace scores;
 // same).
 constexpr int kQRaw = 2;         // staged bf16 query rows
 constexpr int kQSlots = 2;       // split e4m3 query tiles
-constexpr int kAccStages = 4;
+constexpr int kAccStages = 2;
 constexpr int kRing = 16;        // metadata and scale ring, >= S + kAccStages + 1 (a power of two)
 constexpr int kCtasPerSm = 3;
-constexpr int kAccCols = 32;     // N = 32 heads
+constexpr int kAccCols = 64;     // N = 64: the 32 heads' hi terms, then their lo terms
 constexpr uint32_t kTmemCols = kAccStages * kAccCols;  // 128
 constexpr int kSplitWarps = 2;                  // warps 8, 9
 constexpr int kConvThreads = 32 * kSplitWarps;
@@ -400,16 +404,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const uint64_t a_desc = smem_desc_kmajor_sw64(smem_u32(tiles + size_t(stage) * kStageBytes));
                     const uint8_t* qt = q8 + size_t(q_used % kQSlots) * kQ8Bytes;
                     const uint64_t b_hi = smem_desc_kmajor_sw64(smem_u32(qt));
-                    const uint64_t b_lo = smem_desc_kmajor_sw64(smem_u32(qt + kQHalfBytes));
                     const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
-                    // K = 32 codes per MMA: +32 bytes = +2 in the address field.  hi, then lo,
-                    // against the same two K-slices of the keys, into one accumulator.
+                    // K = 32 codes per MMA: +32 bytes = +2 in the address field.  The lo tile
+                    // follows the hi tile (rows 32..63 of one N = 64 operand: with 64-byte rows the
+                    // swizzle pattern repeats every 8 rows, so the two 32-row tiles are one tile).
 #pragma unroll
                     for (int kk = 0; kk < kHeadDim / 32; ++kk)
                         umma_f8_ss(d_tmem, a_desc + 2u * kk, b_hi + 2u * kk, kIdesc, kk > 0 ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < kHeadDim / 32; ++kk)
-                        umma_f8_ss(d_tmem, a_desc + 2u * kk, b_lo + 2u * kk, kIdesc, 1u);
                     umma_commit(&ctl.empty[stage]);
                     umma_commit(&ctl.tfull[acc]);
                 }
@@ -563,19 +564,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * kAccCols);
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
             {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr, r);  // acc[h], h = 0..31
-                tmem_ld_wait(r);
-                tc_fence_before_sync();
-                mbar_arrive(&ctl.tempty[acc]);
                 const float4* w4 = reinterpret_cast<const float4*>(wv);
 #pragma unroll
-                for (int h4 = 0; h4 < kHeads / 4; ++h4) {
-                    const float4 wq = w4[h4];
-                    fma2(s0, s1, wq.x, wq.y, fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f),
-                         fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f));
-                    fma2(s2, s3, wq.z, wq.w, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f),
-                         fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f));
+                for (int half = 0; half < 2; ++half) {  // heads 16 half .. 16 half + 15
+                    uint32_t hi[16], lo[16];
+                    tmem_ld_32x32b_x16(taddr + uint32_t(16 * half), hi);
+                    tmem_ld_32x32b_x16(taddr + uint32_t(kHeads + 16 * half), lo);
+                    tmem_ld_wait16(hi);
+                    tmem_ld_wait16(lo);
+                    if (half == 1) {
+                        tc_fence_before_sync();
+                        mbar_arrive(&ctl.tempty[acc]);
+                    }
+#pragma unroll
+                    for (int h4 = 0; h4 < 4; ++h4) {
+                        const float4 wq = w4[4 * half + h4];
+                        const float a0 = __uint_as_float(hi[4 * h4 + 0]) + __uint_as_float(lo[4 * h4 + 0]);
+                        const float a1 = __uint_as_float(hi[4 * h4 + 1]) + __uint_as_float(lo[4 * h4 + 1]);
+                        const float a2 = __uint_as_float(hi[4 * h4 + 2]) + __uint_as_float(lo[4 * h4 + 2]);
+                        const float a3 = __uint_as_float(hi[4 * h4 + 3]) + __uint_as_float(lo[4 * h4 + 3]);
+                        fma2(s0, s1, wq.x, wq.y, fmaxf(a0, 0.f), fmaxf(a1, 0.f));
+                        fma2(s2, s3, wq.z, wq.w, fmaxf(a2, 0.f), fmaxf(a3, 0.f));
+                    }
                 }
             }
             const float s = key_scale * ((s0 + s1) + (s2 + s3));
